@@ -1,0 +1,384 @@
+/*
+ * wql_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow CPU restatement of the weight-only quantised lm_head path.
+ * Only the tests, the smoke check and the bench's CPU-baseline leg may load
+ * it; the product library never links, loads or calls anything here, and
+ * this file includes nothing from the product sources.
+ *
+ * What it follows (page titles and sections):
+ *  - radiance_lmhead_int4.py, module constants and quantize_int4_rows():
+ *    symmetric per-group int4, q in [-8, 7], scale from amax times r/7,
+ *    clamped below at 1e-8, rounded to the storage dtype BEFORE q is chosen,
+ *    q = round-half-even(w / s) clamped, nibble = q + 8; with the "mse" clip
+ *    the ratios 1.0, 0.95, 0.9, 0.85, 0.8 are tried in that order and a
+ *    ratio replaces the kept one only when its squared error is strictly
+ *    smaller.
+ *  - "Fused WNA16 GEMM for tied quantized lm_head logits", Purpose: the
+ *    weight is packed along the hidden (input) dimension; the logits are
+ *    X . dequant(Wq)^T.  Perf-evals table rows "W8-g128" and the reviewer
+ *    comment (item 1) for int8 weights with per-group or per-row scales.
+ *  - same page, reviewer comment item 2: take the top-K of the quantised
+ *    logits, recompute those K rows exactly from the unquantised weight and
+ *    scatter them back.
+ *
+ * Arithmetic (where the pages leave a step open, the reading is stated):
+ *  - scale:   s = RN_sdtype(max(fl32(amax) *f32 fl32(r/qmax), 1e-8f)),
+ *             qmax = 7 (int4) or 127 (int8); RTN uses r = 1.0 only.
+ *  - code:    q = clamp(rint_even(w_f32 /f32 s_f32), qmin, qmax); if the
+ *             rounded scale is zero (fp16 underflow) the group's q are all 0.
+ *  - MSE:     err_r = sum over the group, k ascending, of (q*s - w)^2 in
+ *             binary64, added one term at a time.
+ *  - logits:  sum_k x[m,k] * (q[n,k] * s[n,g(k)]) in binary64, k ascending,
+ *             plus bias[n]; A[m,n] = sum_k |x[m,k] * w[n,k]| is returned for
+ *             the tolerance 1e-3 + 2e-3 * A.
+ *  - top-K:   value descending, index ascending on equal values.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fPIC -shared -pthread (no fast-math),
+ * so every float operation is the IEEE operation written.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
+
+/* ------------------------------------------------------------------------ */
+/* binary16 / bfloat16 <-> binary64, written from the IEEE 754 definitions.  */
+/* ------------------------------------------------------------------------ */
+
+/* Round the finite double |v| to a binary format with `p` significant bits,
+ * minimum normal exponent `emin` and maximum exponent `emax`, ties to even.
+ * Returns +inf on overflow. */
+static double round_to_format(double v, int p, int emin, int emax) {
+  double a = fabs(v);
+  if (a == 0.0) return 0.0;
+  int e;
+  frexp(a, &e);          /* a = f * 2^e, f in [0.5, 1) -> exponent e-1 */
+  int ex = e - 1;
+  if (ex < emin) ex = emin;             /* subnormal range: fixed quantum */
+  double quantum = ldexp(1.0, ex - (p - 1));
+  double units = a / quantum;           /* exact: power-of-two scaling */
+  double r = nearbyint(units);          /* default mode: ties to even */
+  double out = r * quantum;
+  /* largest finite: (2 - 2^(1-p)) * 2^emax */
+  double maxfin = ldexp(2.0 - ldexp(1.0, 1 - p), emax);
+  if (out > maxfin) return INFINITY;
+  return out;
+}
+
+static uint16_t encode_format(double v_signed, int p, int emin, int emax,
+                              int expbits) {
+  int neg = signbit(v_signed) ? 1 : 0;
+  double a = fabs(v_signed);
+  uint32_t sign = (uint32_t)neg << 15;
+  int mbits = p - 1;
+  int bias = (1 << (expbits - 1)) - 1;
+  if (isnan(v_signed)) return (uint16_t)(sign | (((1u << expbits) - 1) << mbits) | (1u << (mbits - 1)));
+  if (isinf(a)) return (uint16_t)(sign | (((1u << expbits) - 1) << mbits));
+  if (a == 0.0) return (uint16_t)sign;
+  int e;
+  frexp(a, &e);
+  int ex = e - 1;
+  if (ex < emin) { /* subnormal */
+    double units = a / ldexp(1.0, emin - mbits);
+    return (uint16_t)(sign | (uint32_t)units);
+  }
+  double frac = a / ldexp(1.0, ex) - 1.0;         /* in [0, 1) */
+  uint32_t mant = (uint32_t)(frac * (double)(1u << mbits));
+  (void)emax;
+  return (uint16_t)(sign | ((uint32_t)(ex + bias) << mbits) | mant);
+}
+
+uint16_t oracle_f32_to_f16(float f) {
+  double v = (double)f;
+  if (isnan(v)) return encode_format(v, 11, -14, 15, 5);
+  double r = round_to_format(v, 11, -14, 15);
+  return encode_format(copysign(r, v), 11, -14, 15, 5);
+}
+
+uint16_t oracle_f32_to_bf16(float f) {
+  double v = (double)f;
+  if (isnan(v)) return encode_format(v, 8, -126, 127, 8);
+  double r = round_to_format(v, 8, -126, 127);
+  return encode_format(copysign(r, v), 8, -126, 127, 8);
+}
+
+static double decode_format(uint16_t bits, int mbits, int expbits) {
+  int neg = (bits >> 15) & 1;
+  uint32_t e = (bits >> mbits) & ((1u << expbits) - 1);
+  uint32_t mant = bits & ((1u << mbits) - 1);
+  int bias = (1 << (expbits - 1)) - 1;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)mant, 1 - bias - mbits);
+  } else if (e == (1u << expbits) - 1) {
+    v = mant ? NAN : INFINITY;
+  } else {
+    v = ldexp(1.0 + (double)mant / (double)(1u << mbits), (int)e - bias);
+  }
+  return neg ? -v : v;
+}
+
+double oracle_f16_to_f64(uint16_t b) { return decode_format(b, 10, 5); }
+double oracle_bf16_to_f64(uint16_t b) { return decode_format(b, 7, 8); }
+
+static double load_elem(const void* base, int dtype, int64_t i) {
+  switch (dtype) {
+    case OR_F32: return (double)((const float*)base)[i];
+    case OR_F16: return oracle_f16_to_f64(((const uint16_t*)base)[i]);
+    default:     return oracle_bf16_to_f64(((const uint16_t*)base)[i]);
+  }
+}
+
+static uint16_t store_scale(float s, int scale_dtype) {
+  return scale_dtype == OR_F16 ? oracle_f32_to_f16(s) : oracle_f32_to_bf16(s);
+}
+
+static double scale_value(uint16_t bits, int scale_dtype) {
+  return scale_dtype == OR_F16 ? oracle_f16_to_f64(bits) : oracle_bf16_to_f64(bits);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantiser (radiance_lmhead_int4.py, quantize_int4_rows; int8 variant).    */
+/* ------------------------------------------------------------------------ */
+
+static const double kClipRatios[5] = {1.0, 0.95, 0.9, 0.85, 0.8};
+
+/* w: n*k values (row-major) of w_dtype.  group == 0 means one scale per row.
+ * q_out: n*k signed codes.  scales_out: n*(k/group) storage-dtype bits.
+ * ratio_out (nullable): index of the chosen clip ratio per group.
+ * Returns 0, or -1 on bad arguments. */
+int oracle_quantize(const void* w, int w_dtype, int64_t n, int64_t k, int bits,
+                    int group, int scale_dtype, int clip, int8_t* q_out,
+                    uint16_t* scales_out, int8_t* ratio_out) {
+  if (bits != 4 && bits != 8) return -1;
+  int64_t g = group == 0 ? k : group;
+  if (g <= 0 || k % g != 0) return -1;
+  const int qmax = bits == 4 ? 7 : 127;
+  const int qmin = bits == 4 ? -8 : -127;
+  const int nratios = clip ? 5 : 1;
+  const int64_t ngroups = k / g;
+  int8_t* qtry = (int8_t*)malloc((size_t)g);
+  if (!qtry) return -1;
+  for (int64_t row = 0; row < n; ++row) {
+    for (int64_t gi = 0; gi < ngroups; ++gi) {
+      const int64_t base = row * k + gi * g;
+      /* amax over the group, in fp32 (exact: max of magnitudes) */
+      float amax = 0.0f;
+      for (int64_t j = 0; j < g; ++j) {
+        float a = fabsf((float)load_elem(w, w_dtype, base + j));
+        if (a > amax) amax = a;
+      }
+      double best_err = 0.0;
+      int best_r = -1;
+      uint16_t best_sbits = 0;
+      for (int ri = 0; ri < nratios; ++ri) {
+        float c = (float)(kClipRatios[ri] / (double)qmax);
+        float prod = amax * c;                      /* fp32, round to nearest */
+        if (prod < 1e-8f) prod = 1e-8f;             /* zero-group guard */
+        uint16_t sbits = store_scale(prod, scale_dtype);
+        float s = (float)scale_value(sbits, scale_dtype); /* exact widening */
+        double err = 0.0;
+        for (int64_t j = 0; j < g; ++j) {
+          float wv = (float)load_elem(w, w_dtype, base + j);
+          int q;
+          if (s == 0.0f) {
+            q = 0;
+          } else {
+            float t = wv / s;                       /* IEEE fp32 division */
+            float rq = rintf(t);                    /* ties to even */
+            if (rq > (float)qmax) rq = (float)qmax;
+            if (rq < (float)qmin) rq = (float)qmin;
+            q = (int)rq;
+          }
+          qtry[j] = (int8_t)q;
+          if (nratios > 1) {
+            double d = (double)q * (double)s - (double)wv;
+            err = err + d * d;
+          }
+        }
+        if (best_r < 0 || err < best_err) {
+          best_err = err;
+          best_r = ri;
+          best_sbits = sbits;
+          memcpy(q_out + base, qtry, (size_t)g);
+        }
+      }
+      scales_out[row * ngroups + gi] = best_sbits;
+      if (ratio_out) ratio_out[row * ngroups + gi] = (int8_t)best_r;
+    }
+  }
+  free(qtry);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Packing: element k = 8i + j of a row sits in bits [4j, 4j+4) of word i.   */
+/* ------------------------------------------------------------------------ */
+
+int oracle_pack_int4(const uint8_t* nib, int64_t n, int64_t k, uint32_t* packed) {
+  if (k % 8 != 0) return -1;
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t i = 0; i < k / 8; ++i) {
+      uint32_t word = 0;
+      for (int j = 0; j < 8; ++j)
+        word |= ((uint32_t)(nib[r * k + 8 * i + j] & 15u)) << (4 * j);
+      packed[r * (k / 8) + i] = word;
+    }
+  return 0;
+}
+
+int oracle_unpack_int4(const uint32_t* packed, int64_t n, int64_t k, uint8_t* nib) {
+  if (k % 8 != 0) return -1;
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t kk = 0; kk < k; ++kk) {
+      uint32_t word = packed[r * (k / 8) + kk / 8];
+      nib[r * k + kk] = (uint8_t)((word >> (4 * (kk % 8))) & 15u);
+    }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Logits in binary64 from the packed weight (explicit unpack + dequant).    */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const void* x; int x_dtype; int64_t m, k;
+  const void* qweight; int bits;
+  const uint16_t* scales; int scale_dtype; int64_t group;
+  int64_t n; const void* bias; int bias_dtype;
+  const int64_t* rows; int64_t nrows;
+  double* out; double* abs_out;
+  int64_t r_begin, r_end;
+} logits_job;
+
+static double dequant(const logits_job* J, int64_t row, int64_t kk) {
+  int q;
+  if (J->bits == 4) {
+    const uint32_t* P = (const uint32_t*)J->qweight;
+    uint32_t word = P[row * (J->k / 8) + kk / 8];
+    int nibble = (int)((word >> (4 * (kk % 8))) & 15u);
+    q = nibble - 8;
+  } else {
+    q = (int)((const int8_t*)J->qweight)[row * J->k + kk];
+  }
+  int64_t ngroups = J->k / J->group;
+  double s = scale_value(J->scales[row * ngroups + kk / J->group], J->scale_dtype);
+  return (double)q * s;
+}
+
+static void* logits_worker(void* arg) {
+  const logits_job* J = (const logits_job*)arg;
+  for (int64_t ri = J->r_begin; ri < J->r_end; ++ri) {
+    int64_t row = J->rows ? J->rows[ri] : ri;
+    for (int64_t mi = 0; mi < J->m; ++mi) {
+      double acc = 0.0, absacc = 0.0;
+      for (int64_t kk = 0; kk < J->k; ++kk) {
+        double xv = load_elem(J->x, J->x_dtype, mi * J->k + kk);
+        double p = xv * dequant(J, row, kk);
+        acc = acc + p;
+        absacc = absacc + fabs(p);
+      }
+      if (J->bias) acc = acc + load_elem(J->bias, J->bias_dtype, row);
+      J->out[mi * J->nrows + ri] = acc;
+      if (J->abs_out) J->abs_out[mi * J->nrows + ri] = absacc;
+    }
+  }
+  return NULL;
+}
+
+/* x: [m, k] of x_dtype.  qweight: bits 4 -> uint32 [n, k/8]; bits 8 -> int8
+ * [n, k].  scales: [n, k/group] (group 0 = per row).  bias: nullable [n].
+ * rows: nullable list of nrows vocab rows; when NULL, nrows must equal n.
+ * out / abs_out: [m, nrows].  nthreads >= 1 splits the rows. */
+int oracle_logits(const void* x, int x_dtype, int64_t m, int64_t k,
+                  const void* qweight, int bits, const uint16_t* scales,
+                  int scale_dtype, int group, int64_t n, const void* bias,
+                  int bias_dtype, const int64_t* rows, int64_t nrows,
+                  double* out, double* abs_out, int nthreads) {
+  int64_t g = group == 0 ? k : group;
+  if ((bits != 4 && bits != 8) || g <= 0 || k % g != 0) return -1;
+  if (bits == 4 && k % 8 != 0) return -1;
+  if (!rows && nrows != n) return -1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  logits_job base = {x, x_dtype, m, k, qweight, bits, scales, scale_dtype, g,
+                     n, bias, bias_dtype, rows, nrows, out, abs_out, 0, 0};
+  pthread_t th[256];
+  int joined[256];
+  logits_job jobs[256];
+  int64_t per = (nrows + nthreads - 1) / nthreads;
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = base;
+    jobs[t].r_begin = t * per < nrows ? t * per : nrows;
+    jobs[t].r_end = (t + 1) * per < nrows ? (t + 1) * per : nrows;
+    joined[t] = 0;
+    if (nthreads == 1 || pthread_create(&th[t], NULL, logits_worker, &jobs[t]) != 0) {
+      logits_worker(&jobs[t]);   /* run inline if no thread could be made */
+      joined[t] = 1;
+    }
+  }
+  for (int t = 0; t < nthreads; ++t)
+    if (!joined[t]) pthread_join(th[t], NULL);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Top-K (value desc, index asc) and exact rescoring of chosen rows.         */
+/* ------------------------------------------------------------------------ */
+
+int oracle_topk(const double* vals, int64_t m, int64_t n, int K,
+                int32_t* idx_out, double* val_out) {
+  if (K < 1) return -1;
+  for (int64_t mi = 0; mi < m; ++mi) {
+    int have = 0;
+    for (int64_t j = 0; j < n; ++j) {
+      double v = vals[mi * n + j];
+      if (isnan(v)) continue;
+      /* position where (v, j) belongs: after every entry that ranks higher */
+      int pos = have;
+      while (pos > 0) {
+        double pv = val_out[mi * K + pos - 1];
+        if (pv > v || (pv == v && idx_out[mi * K + pos - 1] < j)) break;
+        --pos;
+      }
+      if (pos >= K) continue;
+      int last = have < K ? have : K - 1;
+      for (int t = last; t > pos; --t) {
+        val_out[mi * K + t] = val_out[mi * K + t - 1];
+        idx_out[mi * K + t] = idx_out[mi * K + t - 1];
+      }
+      val_out[mi * K + pos] = v;
+      idx_out[mi * K + pos] = (int32_t)j;
+      if (have < K) ++have;
+    }
+    for (int t = have; t < K; ++t) { val_out[mi * K + t] = -INFINITY; idx_out[mi * K + t] = -1; }
+  }
+  return 0;
+}
+
+/* out[m, K] = sum_k x[m,k] * wref[idx[m,K], k] (+ bias[idx]) in binary64. */
+int oracle_rescore(const void* x, int x_dtype, int64_t m, int64_t k,
+                   const void* wref, int wref_dtype, int64_t n,
+                   const int32_t* idx, int K, const void* bias, int bias_dtype,
+                   double* out, double* abs_out) {
+  for (int64_t mi = 0; mi < m; ++mi)
+    for (int t = 0; t < K; ++t) {
+      int64_t row = idx[mi * K + t];
+      if (row < 0 || row >= n) return -1;
+      double acc = 0.0, absacc = 0.0;
+      for (int64_t kk = 0; kk < k; ++kk) {
+        double p = load_elem(x, x_dtype, mi * k + kk) *
+                   load_elem(wref, wref_dtype, row * k + kk);
+        acc = acc + p;
+        absacc = absacc + fabs(p);
+      }
+      if (bias) acc = acc + load_elem(bias, bias_dtype, row);
+      out[mi * K + t] = acc;
+      if (abs_out) abs_out[mi * K + t] = absacc;
+    }
+  return 0;
+}

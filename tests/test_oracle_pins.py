@@ -1,0 +1,373 @@
+"""Pins for the CPU oracle: each test ties it to something other than itself.
+
+* IEEE conversions against numpy (binary16) and torch (bfloat16) rounding;
+* the packed layout against hand-written worked examples (tests/golden);
+* the quantiser against a hand-worked example, a brute-force nearest-integer
+  search in exact rational arithmetic, library fp16/bf16 rounding of the
+  scale, closed-form invariants and exact-arithmetic MSE minimality;
+* logits against a dense numpy fp64 product built before packing, and closed
+  forms (unit vectors, zero weight, one live group, constant codes);
+* top-K against a numpy lexsort brute force; rescoring against numpy dots.
+"""
+from fractions import Fraction
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import F32, F16, BF16
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@np.errstate(over="ignore")
+def _f16_bits(a):
+    return np.asarray(a, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def _bf16_bits(a):
+    t = torch.tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _edge_floats():
+    vals = [0.0, -0.0, 1.0, -1.0, 65504.0, 65519.99, 65520.0, 65536.0, 1e9, -1e9,
+            2.0 ** -14, 2.0 ** -24, 2.0 ** -25, 2.0 ** -25 * 1.0000001, 3 * 2.0 ** -26,
+            2.0 ** -126, 2.0 ** -133, 2.0 ** -134, 1e-8, -1e-8, 3.4e38, 1.0009765625,
+            1.00048828125, 1.00146484375, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -9, 255.5, 256.5]
+    return np.array(vals, dtype=np.float32)
+
+
+def _random_floats(n, seed):
+    rng = np.random.default_rng(seed)
+    mant = rng.uniform(-2.0, 2.0, n)
+    ex = rng.integers(-30, 20, n)
+    v = (mant * np.exp2(ex)).astype(np.float32)
+    # exact binary16 / bfloat16 ties: halfway between two neighbours
+    base = rng.uniform(-100, 100, n // 8).astype(np.float16).astype(np.float32)
+    ties16 = base + np.abs(base) * np.float32(2.0 ** -11)
+    return np.concatenate([v, ties16.astype(np.float32)])
+
+
+# --------------------------------------------------------------------------
+# conversions
+# --------------------------------------------------------------------------
+
+def test_f16_rounding_matches_numpy(oracle_mod):
+    v = np.concatenate([_edge_floats(), _random_floats(20000, 0)])
+    np.testing.assert_array_equal(oracle.f32_to_f16_bits(v), _f16_bits(v))
+
+
+def test_bf16_rounding_matches_torch(oracle_mod):
+    v = np.concatenate([_edge_floats(), _random_floats(20000, 1)])
+    np.testing.assert_array_equal(oracle.f32_to_bf16_bits(v), _bf16_bits(v))
+
+
+def test_f16_decode_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint16)
+    ours = oracle.f16_bits_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(ours[ok], ref[ok])
+
+
+def test_bf16_decode_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint16)
+    ours = oracle.bf16_bits_to_f64(bits)
+    ref = torch.tensor(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(ours[ok], ref[ok])
+
+
+# --------------------------------------------------------------------------
+# packing
+# --------------------------------------------------------------------------
+
+def _read_pack_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "pack_int4.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            lhs, rhs = line.split("->")
+            cases.append(([int(t) for t in lhs.split()], int(rhs.strip(), 16)))
+    return cases
+
+
+def test_pack_worked_examples(oracle_mod):
+    cases = _read_pack_golden()
+    assert len(cases) >= 5
+    nib = np.array([c[0] for c in cases], dtype=np.uint8)
+    words = oracle.pack_int4(nib).view(np.uint32)[:, 0]
+    np.testing.assert_array_equal(words, np.array([c[1] for c in cases], dtype=np.uint32))
+
+
+def test_pack_every_value_every_position(oracle_mod):
+    rows = []
+    expect = []
+    for j in range(8):
+        for v in range(16):
+            r = [0] * 8
+            r[j] = v
+            rows.append(r)
+            expect.append(v << (4 * j))
+    words = oracle.pack_int4(np.array(rows, dtype=np.uint8)).view(np.uint32)[:, 0]
+    np.testing.assert_array_equal(words, np.array(expect, dtype=np.uint32))
+
+
+def test_pack_unpack_roundtrip(oracle_mod):
+    rng = np.random.default_rng(3)
+    nib = rng.integers(0, 16, (37, 96), dtype=np.uint8)
+    packed = oracle.pack_int4(nib)
+    assert packed.shape == (37, 12) and packed.dtype == np.int32
+    np.testing.assert_array_equal(oracle.unpack_int4(packed, 96), nib)
+
+
+# --------------------------------------------------------------------------
+# quantiser
+# --------------------------------------------------------------------------
+
+def test_quantize_worked_example(oracle_mod):
+    lines = {}
+    with open(os.path.join(GOLDEN, "quant_rtn_worked.txt")) as f:
+        for line in f:
+            if line.startswith("#") or ":" not in line:
+                continue
+            key, val = line.split(":", 1)
+            lines[key.strip()] = val.split()
+    w = np.array([float(t) for t in lines["w"]], dtype=np.float32)[None, :]
+    q, s, _ = oracle.quantize(w, F32, 4, 8, F16, 0)
+    assert int(s[0, 0]) == int(lines["scale_f16_hex"][0], 16)
+    np.testing.assert_array_equal(q[0], np.array([int(t) for t in lines["q"]]))
+    np.testing.assert_array_equal((q[0].astype(np.int32) + 8),
+                                  np.array([int(t) for t in lines["nibbles"]]))
+
+
+def _nearest_int_half_even(t: Fraction, lo: int, hi: int) -> int:
+    """Brute force: the integer in [lo, hi] nearest to t, ties to the even one."""
+    best = None
+    for q in range(lo, hi + 1):
+        d = abs(Fraction(q) - t)
+        if best is None or d < best[0] or (d == best[0] and q % 2 == 0):
+            best = (d, q)
+    return best[1]
+
+
+def _scale_lib(amax: np.float32, r: float, qmax: int, sdt: int) -> np.float32:
+    prod = np.float32(amax) * np.float32(r / qmax)     # numpy fp32 multiply (IEEE)
+    prod = max(prod, np.float32(1e-8))
+    if sdt == F16:
+        return np.float32(np.float16(prod))
+    return np.float32(torch.tensor(float(prod), dtype=torch.float32).to(torch.bfloat16).item())
+
+
+@pytest.mark.parametrize("bits,group,sdt,wdt", [(4, 64, F16, F32), (4, 128, BF16, BF16),
+                                                (8, 128, F16, F32), (8, 0, F16, F16)])
+def test_quantize_rtn_brute_force(oracle_mod, bits, group, sdt, wdt):
+    rng = np.random.default_rng(10 + bits)
+    n, k = 6, 256
+    w32 = (rng.standard_normal((n, k)) * 0.02).astype(np.float32)
+    w32[2, :] = 0.0                                    # an all-zero (padded) row
+    wt = torch.tensor(w32)
+    if wdt == F16:
+        warr = wt.half().numpy()
+        wval = warr.astype(np.float32)
+    elif wdt == BF16:
+        wb = wt.to(torch.bfloat16)
+        warr = wb.view(torch.int16).numpy().view(np.uint16)
+        wval = wb.float().numpy()
+    else:
+        warr = w32
+        wval = w32
+    q, s, _ = oracle.quantize(warr, wdt, bits, group, sdt, 0)
+    g = k if group == 0 else group
+    qmax = 7 if bits == 4 else 127
+    qmin = -8 if bits == 4 else -127
+    sv = oracle.scales_to_f64(s, sdt)
+    for r in range(n):
+        for gi in range(k // g):
+            blk = wval[r, gi * g:(gi + 1) * g]
+            amax = np.float32(np.max(np.abs(blk)))
+            s_lib = _scale_lib(amax, 1.0, qmax, sdt)
+            assert sv[r, gi] == float(s_lib), (r, gi)
+            for j in range(g):
+                if s_lib == 0:
+                    assert q[r, gi * g + j] == 0
+                    continue
+                t = Fraction(float(np.float32(blk[j]) / np.float32(s_lib)))  # IEEE fp32 divide
+                assert q[r, gi * g + j] == _nearest_int_half_even(t, qmin, qmax)
+            if amax > 0:
+                j = int(np.argmax(np.abs(blk)))
+                assert abs(int(q[r, gi * g + j])) == qmax      # RTN maps amax to +-qmax
+    assert np.all(q[2] == 0)                                     # zero group -> zero codes
+    assert q.min() >= qmin and q.max() <= qmax
+
+
+def _exact_err(q, s, w):
+    return sum((Fraction(int(qi)) * Fraction(float(s)) - Fraction(float(wi))) ** 2
+               for qi, wi in zip(q, w))
+
+
+def test_quantize_mse_is_minimal_over_clip_grid(oracle_mod):
+    rng = np.random.default_rng(7)
+    n, k, g = 4, 256, 128
+    w32 = (rng.standard_normal((n, k)) * 0.02).astype(np.float32)
+    w32[1, :5] *= 12.0                                  # outliers make clipping pay
+    wb = torch.tensor(w32).to(torch.bfloat16)
+    warr = wb.view(torch.int16).numpy().view(np.uint16)
+    wval = wb.float().numpy()
+    q, s, ridx = oracle.quantize(warr, BF16, 4, g, BF16, 1)
+    q_rtn, s_rtn, _ = oracle.quantize(warr, BF16, 4, g, BF16, 0)
+    sv = oracle.scales_to_f64(s, BF16)
+    chose_clipped = 0
+    for r in range(n):
+        for gi in range(k // g):
+            blk = wval[r, gi * g:(gi + 1) * g]
+            amax = np.float32(np.max(np.abs(blk)))
+            errs = []
+            for ratio in oracle.CLIP_RATIOS:
+                s_r = _scale_lib(amax, ratio, 7, BF16)
+                q_r = [_nearest_int_half_even(Fraction(float(np.float32(b) / s_r)), -8, 7)
+                       for b in blk]
+                errs.append(_exact_err(q_r, s_r, blk))
+            best = min(range(5), key=lambda i: (errs[i], i))
+            assert ridx[r, gi] == best
+            assert sv[r, gi] == float(_scale_lib(amax, oracle.CLIP_RATIOS[best], 7, BF16))
+            chosen = _exact_err(q[r, gi * g:(gi + 1) * g], sv[r, gi], blk)
+            assert chosen == errs[best]
+            assert chosen <= _exact_err(q_rtn[r, gi * g:(gi + 1) * g],
+                                        oracle.scales_to_f64(s_rtn, BF16)[r, gi], blk)
+            chose_clipped += best > 0
+    assert chose_clipped > 0
+
+
+def test_quantize_fp16_scale_underflow_gives_zero_codes(oracle_mod):
+    w = np.zeros((1, 64), dtype=np.float32)
+    w[0, 3] = 1e-9                       # amax/7 underflows in binary16
+    q, s, _ = oracle.quantize(w, F32, 4, 64, F16, 0)
+    assert int(s[0, 0]) == 0 and np.all(q == 0)
+    qb, sb, _ = oracle.quantize(w, F32, 4, 64, BF16, 0)
+    assert oracle.scales_to_f64(sb, BF16)[0, 0] > 0     # 1e-8 survives in bf16
+
+
+def test_quantize_int8_range(oracle_mod):
+    rng = np.random.default_rng(4)
+    w = (rng.standard_normal((8, 256)) * 0.02).astype(np.float32)
+    q, _, _ = oracle.quantize(w, F32, 8, 0, F16, 0)
+    assert q.min() >= -127 and q.max() <= 127
+    assert set(np.abs(q).max(axis=1).tolist()) == {127}
+
+
+# --------------------------------------------------------------------------
+# logits
+# --------------------------------------------------------------------------
+
+def _quantized(n, k, bits, group, sdt, seed=0):
+    rng = np.random.default_rng(seed)
+    w = (rng.standard_normal((n, k)) * 0.02).astype(np.float32)
+    q, s, _ = oracle.quantize(w, F32, bits, group, sdt, 0)
+    if bits == 4:
+        qw = oracle.pack_int4((q.astype(np.int16) + 8).astype(np.uint8))
+    else:
+        qw = q
+    return q, s, qw
+
+
+def _dense(q, s, group, sdt):
+    n, k = q.shape
+    g = k if group == 0 else group
+    sv = oracle.scales_to_f64(s, sdt)
+    return q.astype(np.float64) * np.repeat(sv, g, axis=1)
+
+
+@pytest.mark.parametrize("bits,group,sdt,xdt", [(4, 64, F16, F16), (4, 128, BF16, BF16),
+                                                (8, 128, F16, F16), (8, 0, F16, F16)])
+def test_logits_match_dense_product(oracle_mod, bits, group, sdt, xdt):
+    n, k, m = 45, 256, 3
+    q, s, qw = _quantized(n, k, bits, group, sdt)
+    rng = np.random.default_rng(1)
+    x32 = rng.standard_normal((m, k)).astype(np.float32)
+    if xdt == F16:
+        xarr = x32.astype(np.float16)
+        xval = xarr.astype(np.float64)
+    else:
+        xb = torch.tensor(x32).to(torch.bfloat16)
+        xarr = xb.view(torch.int16).numpy().view(np.uint16)
+        xval = xb.double().numpy()
+    out, absacc = oracle.logits(xarr, xdt, qw, bits, s, sdt, group, n, k)
+    wd = _dense(q, s, group, sdt)
+    ref = xval @ wd.T
+    refabs = np.abs(xval) @ np.abs(wd).T
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12 * refabs.max())
+    np.testing.assert_allclose(absacc, refabs, rtol=1e-12)
+    rows = np.array([44, 0, 7, 7], dtype=np.int64)
+    sub, _ = oracle.logits(xarr, xdt, qw, bits, s, sdt, group, n, k, rows=rows, nthreads=3)
+    np.testing.assert_array_equal(sub, out[:, rows])
+
+
+def test_logits_closed_forms(oracle_mod):
+    n, k, g = 16, 128, 64
+    q, s, qw = _quantized(n, k, 4, g, F16, seed=2)
+    sv = oracle.scales_to_f64(s, F16)
+    # x = e_kk picks column kk of the dequantised weight, exactly
+    for kk in (0, 5, 63, 64, 127):
+        x = np.zeros((1, k), dtype=np.float16)
+        x[0, kk] = 1.0
+        out, _ = oracle.logits(x, F16, qw, 4, s, F16, g, n, k)
+        np.testing.assert_array_equal(out[0], q[:, kk] * sv[:, kk // g])
+    # all-zero codes (nibble 8) give zero logits
+    zero = oracle.pack_int4(np.full((n, k), 8, dtype=np.uint8))
+    x = np.ones((2, k), dtype=np.float16)
+    out, absacc = oracle.logits(x, F16, zero, 4, s, F16, g, n, k)
+    assert np.all(out == 0) and np.all(absacc == 0)
+    # constant code c with x = 1 over one live group: c * s * 64
+    nib = np.full((n, k), 8, dtype=np.uint8)
+    nib[:, 64:] = 8 + 3
+    out, _ = oracle.logits(x, F16, oracle.pack_int4(nib), 4, s, F16, g, n, k)
+    np.testing.assert_array_equal(out[0], 3 * sv[:, 1] * 64)
+    # bias is added once
+    b = np.linspace(-1, 1, n).astype(np.float16)
+    outb, _ = oracle.logits(x, F16, oracle.pack_int4(nib), 4, s, F16, g, n, k, bias=b)
+    np.testing.assert_array_equal(outb[0], out[0] + b.astype(np.float64))
+
+
+# --------------------------------------------------------------------------
+# top-K and rescoring
+# --------------------------------------------------------------------------
+
+def test_topk_matches_lexsort(oracle_mod):
+    rng = np.random.default_rng(11)
+    vals = rng.integers(-20, 20, (5, 300)).astype(np.float64)   # many exact ties
+    vals[2, :] = 1.0
+    for K in (1, 4, 8, 16):
+        idx, val = oracle.topk(vals, K)
+        for r in range(vals.shape[0]):
+            order = np.lexsort((np.arange(vals.shape[1]), -vals[r]))[:K]
+            np.testing.assert_array_equal(idx[r], order)
+            np.testing.assert_array_equal(val[r], vals[r, order])
+    small, _ = oracle.topk(vals[:, :3], 5)
+    assert np.all(small[:, 3:] == -1)
+
+
+def test_rescore_matches_numpy_dot(oracle_mod):
+    rng = np.random.default_rng(12)
+    n, k, m, K = 50, 64, 3, 8
+    wref = (rng.standard_normal((n, k)) * 0.02).astype(np.float16)
+    x = rng.standard_normal((m, k)).astype(np.float16)
+    idx = rng.integers(0, n, (m, K)).astype(np.int32)
+    out, absacc = oracle.rescore(x, F16, wref, F16, idx)
+    for r in range(m):
+        for t in range(K):
+            ref = np.dot(x[r].astype(np.float64), wref[idx[r, t]].astype(np.float64))
+            assert abs(out[r, t] - ref) <= 1e-13
+    # a planted large row wins the argmax
+    wref[17] = 1.0
+    x = np.abs(x)
+    idx[:, 0] = 17
+    out, _ = oracle.rescore(x, F16, wref, F16, idx)
+    assert np.all(np.argmax(out, axis=1) == 0)
