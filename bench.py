@@ -1,0 +1,458 @@
+"""Benchmark: W4/W8 lm_head logits (+ top-8, + exact rescoring) on one GB300.
+
+One step = one pass of the hot path over the 151936 x 1024 W4-g64 head
+("Fused WNA16 GEMM for tied quantized lm_head logits", Perf evals table):
+for each M in (1, 32, 256), wql_logits with top-8 candidates followed by
+wql_topk_rescore of those candidates from the fp16 reference rows.
+Quantisation (load time) is timed once, outside the steps.
+
+Timing: CUDA events on the launching stream around every call, L2 flushed
+(a 512 MB write) before every call, outside the events; `value` is the
+algorithmic bytes of the step (packed weight + scales + X + logits written
++ rescored rows) over the summed device time.  `--gpus N` under torchrun runs
+N independent replicas (the head is replicated, not sharded) and reports the
+units of all ranks over the slowest rank's time.
+
+`--impl reference` times the CPU oracle (the slow binary64 C restatement) on
+a bounded row sample of the same workload and prints the same JSON line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+N_VOCAB, K_HIDDEN, GROUP, TOPK = 151936, 1024, 64, 8
+MS = (1, 32, 256)
+WORKLOAD = "lm_head 151936x1024 W4-g64 RTN fp16-scale, X fp16 at M=1/32/256, top-8 + rescore"
+METRIC = "HBM GB/s and us/call of W4/W8 lm_head logits at M=1/32/256 (% of roofline)"
+L2_FLUSH_BYTES = 512 * 2**20
+
+
+# ---------------------------------------------------------------------------
+# byte / flop accounting (what the method itself must move)
+# ---------------------------------------------------------------------------
+
+def logits_bytes(m: int, n: int, k: int, bits: int, group: int, out_bytes: int = 2,
+                 x_bytes: int = 2, scale_bytes: int = 2, topk: int = 0) -> int:
+    """Packed weight + scale table + X read + logits written (+ top-K out)."""
+    g = k if group == 0 else group
+    w = n * k * bits // 8
+    s = n * (k // g) * scale_bytes
+    return w + s + m * k * x_bytes + m * n * out_bytes + m * topk * 8
+
+
+def rescore_bytes(m: int, k: int, topk: int, w_bytes: int = 2, x_bytes: int = 2) -> int:
+    """The K reference rows read per token row (+ x, + values written back)."""
+    return m * topk * k * w_bytes + m * k * x_bytes + m * topk * (8 + 2)
+
+
+def step_bytes() -> int:
+    return sum(logits_bytes(m, N_VOCAB, K_HIDDEN, 4, GROUP, topk=TOPK) +
+               rescore_bytes(m, K_HIDDEN, TOPK) for m in MS)
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_src_hash(names) -> str:
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "weight_only_quantized_wql_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, src_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    this exact kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        if line.startswith("#") or "=" not in line:
+            continue
+        kv = dict(tok.split("=", 1) for tok in line.split())
+        if kv.get("kernel") == kernel and kv.get("workload") == workload and \
+                kv.get("src") == src_hash:
+            return int(kv["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+    import weight_only_quantized_wql_gb300 as wql
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wql.load()
+    stream = torch.cuda.current_stream(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    w = torch.randn(N_VOCAB, K_HIDDEN, generator=gen, device=dev).mul_(0.02)
+    w_ref = w.half()
+    xs = {}
+    for m in MS:
+        g2 = torch.Generator(device=dev)
+        g2.manual_seed(1000 + m)
+        xs[m] = torch.randn(m, K_HIDDEN, generator=g2, device=dev).half()
+    # load-time quantisation, timed once
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    qw = wql.wql_quantize(w, 4, GROUP, torch.float16, wql.CLIP_RTN)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    quant_ms = e0.elapsed_time(e1)
+    del w
+    ws = wql.Workspace(dev)
+    outs = {m: torch.empty(m, N_VOCAB, dtype=torch.float16, device=dev) for m in MS}
+    idx = {m: torch.empty(m, TOPK, dtype=torch.int32, device=dev) for m in MS}
+    val = {m: torch.empty(m, TOPK, dtype=torch.float32, device=dev) for m in MS}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def call(m):
+        wql.wql_logits(xs[m], qw, topk=TOPK, workspace=ws, out=outs[m], topk_idx=idx[m],
+                       topk_val=val[m])
+
+    def rescore(m):
+        wql.wql_topk_rescore(xs[m], w_ref, idx[m], val[m], outs[m])
+
+    def one_step(record):
+        per = {}
+        for m in MS:
+            flush.zero_()
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record(stream)
+            call(m)
+            b.record(stream)
+            rescore(m)
+            c.record(stream)
+            per[m] = (a, b, c)
+        return per
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        one_step(False)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = wql.wql_launch_count()
+    t_wall0 = time.perf_counter()
+    recs = [one_step(True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = wql.wql_launch_count() - launches0
+    barrier()
+    clk = clocks.stop()
+
+    logit_us = {m: [] for m in MS}
+    resc_us = {m: [] for m in MS}
+    for per in recs:
+        for m, (a, b, c) in per.items():
+            logit_us[m].append(a.elapsed_time(b) * 1e3)
+            resc_us[m].append(b.elapsed_time(c) * 1e3)
+    step_us = [sum(logit_us[m][i] + resc_us[m][i] for m in MS) for i in range(args.steps)]
+    dev_s = sum(step_us) * 1e-6
+
+    # ---- end to end: pinned host X in, logits + top-K out, every call ----
+    hx = {m: xs[m].cpu().pin_memory() for m in MS}
+    hout = {m: torch.empty(m, N_VOCAB, dtype=torch.float16).pin_memory() for m in MS}
+    hidx = {m: torch.empty(m, TOPK, dtype=torch.int32).pin_memory() for m in MS}
+    hval = {m: torch.empty(m, TOPK, dtype=torch.float32).pin_memory() for m in MS}
+    dx = {m: torch.empty_like(xs[m]) for m in MS}
+    e2e_us = []
+    h2d = sum(hx[m].numel() * 2 for m in MS)
+    d2h = sum(hout[m].numel() * 2 + hidx[m].numel() * 4 + hval[m].numel() * 4 for m in MS)
+    for it in range(args.warmup + args.steps):
+        tot = 0.0
+        for m in MS:
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dx[m].copy_(hx[m], non_blocking=True)
+            wql.wql_logits(dx[m], qw, topk=TOPK, workspace=ws, out=outs[m], topk_idx=idx[m],
+                           topk_val=val[m])
+            wql.wql_topk_rescore(dx[m], w_ref, idx[m], val[m], outs[m])
+            hout[m].copy_(outs[m], non_blocking=True)
+            hidx[m].copy_(idx[m], non_blocking=True)
+            hval[m].copy_(val[m], non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            tot += a.elapsed_time(b) * 1e3
+        if it >= args.warmup:
+            e2e_us.append(tot)
+
+    # ---- reduce over ranks: max time ----
+    vals = torch.tensor([dev_s, sum(e2e_us) * 1e-6, t_wall], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
+    dev_s, e2e_s, t_wall = (float(v) for v in vals.tolist())
+    if rank != 0:
+        return None
+
+    pk = peaks()
+    total_bytes = step_bytes() * args.steps * world
+    value = total_bytes / dev_s / 1e9
+    med = {m: statistics.median(logit_us[m]) for m in MS}
+    calls = {}
+    for m in MS:
+        b = logits_bytes(m, N_VOCAB, K_HIDDEN, 4, GROUP, topk=TOPK)
+        fl = 2.0 * m * N_VOCAB * K_HIDDEN
+        gbs = b / (med[m] * 1e-6) / 1e9
+        tfl = fl / (med[m] * 1e-6) / 1e12
+        calls[f"M{m}"] = {
+            "us_median": round(med[m], 2),
+            "us_p10": round(sorted(logit_us[m])[max(0, len(logit_us[m]) // 10)], 2),
+            "GBps": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
+            "TFLOPs": round(tfl, 2), "frac_tensor": round(tfl / pk["bf16_tflops"], 4),
+            "rescore_us": round(statistics.median(resc_us[m]), 2)}
+    # dominant kernel: the logits call with the largest share of device time
+    dom_m = max(MS, key=lambda m: sum(logit_us[m]))
+    dom_us = statistics.mean(logit_us[dom_m])
+    dom_flops = 2.0 * dom_m * N_VOCAB * K_HIDDEN
+    dom_bytes = logits_bytes(dom_m, N_VOCAB, K_HIDDEN, 4, GROUP, topk=TOPK)
+    kern = "logits_tc" if dom_m > 16 and os.path.exists(os.path.join(
+        ROOT, "weight_only_quantized_wql_gb300", "csrc", "tc_gemm.cu")) else "decode"
+    src = kernel_src_hash(["tc_gemm.cu"] if kern == "logits_tc" else ["decode.cu"])
+    traffic = recorded_traffic(kern, f"M{dom_m}", src)
+    if dom_flops / dom_bytes > 286 and kern == "logits_tc":
+        achieved = dom_flops / (dom_us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
+                "kernel": kern, "call": f"M={dom_m}",
+                "peak_note": f"{pk['source']} bf16 burst; fp16 dense rate is the same"}
+    else:
+        achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
+                "kernel": kern, "call": f"M={dom_m}", "peak_note": f"{pk['source']} copy"}
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dev_s / args.steps * 1e3 / 1.0, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4 x f16 products, f32 accumulate", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n": N_VOCAB, "k": K_HIDDEN, "group": GROUP,
+                   "ms": list(MS), "topk": TOPK, "parallelism": f"replicas x{world}",
+                   "l2": "512 MB flush before every call, outside the events",
+                   "step_bytes": step_bytes()},
+        "calls": calls, "quantize_ms": round(quant_ms, 3),
+        "roofline": roof,
+        "cpu_baseline": None,
+        "e2e": {"value": round(step_bytes() * args.steps * world / e2e_s / 1e9, 1),
+                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "wall_s_timed": round(t_wall, 4),
+        "clocks": clk,
+    }
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(rows: int, nthreads: int, state: dict) -> tuple[float, int]:
+    """One oracle step on the first `rows` vocab rows: logits at M=1/32/256,
+    top-8 over the sampled rows, exact rescoring of the candidates.
+    Returns (seconds, algorithmic bytes of the sampled work)."""
+    import numpy as np
+    import oracle
+    if "qw" not in state:
+        import torch
+        from weight_only_quantized_wql_gb300 import synth
+        w = synth.weight(rows, K_HIDDEN, synth.F32, seed=0)
+        state["w_ref"] = w.half().numpy()
+        state["qw"], state["s"] = oracle.quantize_packed(w.numpy(), oracle.F32, 4, GROUP,
+                                                         oracle.F16, 0, nthreads=nthreads)
+        state["x"] = {m: synth.activations(m, K_HIDDEN, synth.F16, seed=1000 + m).numpy()
+                      for m in MS}
+        del torch
+    t0 = time.perf_counter()
+    nbytes = 0
+    for m in MS:
+        out, _ = oracle.logits(state["x"][m], oracle.F16, state["qw"], 4, state["s"], oracle.F16,
+                               GROUP, rows, K_HIDDEN, nthreads=nthreads)
+        idx, _ = oracle.topk(out, TOPK)
+        oracle.rescore(state["x"][m], oracle.F16, state["w_ref"], oracle.F16, idx)
+        nbytes += logits_bytes(m, rows, K_HIDDEN, 4, GROUP, topk=TOPK) + \
+            rescore_bytes(m, K_HIDDEN, TOPK)
+    return time.perf_counter() - t0, nbytes
+
+
+def cpu_rows_for_budget(nthreads: int, seconds: float, state_probe: dict) -> int:
+    """Size the oracle sample so one step takes about `seconds` of CPU time."""
+    probe = 512
+    dt, _ = oracle_sample_step(probe, nthreads, state_probe)
+    rows = int(probe * seconds / max(dt, 1e-6))
+    return max(probe, min(N_VOCAB, rows // 16 * 16))
+
+
+def cpu_baseline(nthreads: int, seconds: float = 12.0) -> dict:
+    rows = cpu_rows_for_budget(nthreads, seconds, {})
+    dt, nbytes = oracle_sample_step(rows, nthreads, {})
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"first {rows} of {N_VOCAB} vocab rows, M=1/32/256 logits + top-8 + "
+                      f"rescore, binary64 C, {nthreads} threads, {dt:.1f} s"}
+
+
+def run_reference(args) -> dict:
+    nthreads = os.cpu_count() or 1
+    budget = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    rows = cpu_rows_for_budget(nthreads, budget, {})
+    state = {}
+    for _ in range(args.warmup):
+        oracle_sample_step(rows, nthreads, state)
+    tot_s, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = oracle_sample_step(rows, nthreads, state)
+        tot_s += dt
+        tot_b += nb
+    value = tot_b / tot_s / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n": N_VOCAB, "k": K_HIDDEN, "group": GROUP,
+                   "ms": list(MS), "topk": TOPK, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads,
+                         "kind": "oracle",
+                         "sample": f"first {rows} of {N_VOCAB} vocab rows per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+
+def aggregate_over_ranks(local: list[float], world: int, op: str = "max") -> list[float]:
+    """Reduce per-rank timings (max) across the process group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(local, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return t.tolist()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(os.cpu_count() or 1)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,175 @@
+/*
+ * wql.h -- C ABI of the weight-only quantised lm_head library (libwql.so).
+ *
+ * One operation and its load-time preparation:
+ *
+ *   logits[m, n] = sum_k x[m, k] * q[n, k] * s[n, k / G]   (+ bias[n])
+ *
+ * with Wq symmetric int4 (nibble = q + 8, q in [-8, 7]) or int8 (q in
+ * [-127, 127]) and one fp16/bf16 scale per group of G hidden columns or per
+ * row.  The dense weight is never materialised.  Sources:
+ *   - "Fused WNA16 GEMM for tied quantized lm_head logits", Purpose: a fused
+ *     dequant-GEMM on the packed [vocab, hidden] table, weights packed along
+ *     the hidden dimension; Perf evals table: W4-g64 and W8-g128 heads at
+ *     M = 1 / 32 / 256; reviewer comment items 1-2: int8 per-row heads and
+ *     exact top-K rescoring from the unquantised weight.
+ *   - radiance_lmhead_int4.py, quantize_int4_rows and module constants:
+ *     symmetric per-group int4, QMAX 7, nibble bias 8, RTN or MSE clip-ratio
+ *     search over 1.0 / 0.95 / 0.9 / 0.85 / 0.8 of amax / 7, the scale rounded
+ *     to its storage dtype before q is chosen, [N, K/8] int32 packing,
+ *     [N, K/G] scale table; apply(): x flattened to [M, K], optional bias.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates no device memory; scratch space is a caller buffer
+ *     sized by wql_workspace_size().
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy
+ *     default stream).  Results are ready once the stream has reached them.
+ *   - Arguments are checked on the host before anything is launched.  On any
+ *     error nothing is launched and nothing is written.  The library never
+ *     aborts, prints or traps; a failed CUDA launch returns WQL_ECUDA and the
+ *     CUDA error text is kept for wql_last_error() (per host thread).
+ *   - Row-major, densely packed tensors.  Sizes are element counts.
+ *   - Empty work (m == 0 or n == 0) returns WQL_OK without launching.
+ */
+#ifndef WQL_H_
+#define WQL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum wql_status {
+  WQL_OK = 0,
+  WQL_EINVAL = 1,        /* null pointer, negative size, inconsistent args */
+  WQL_EUNSUPPORTED = 2,  /* valid but not implemented here (dtype, group, K,
+                            alignment) */
+  WQL_ECUDA = 3,         /* a CUDA call failed; see wql_last_error() */
+  WQL_EWORKSPACE = 4     /* workspace missing or smaller than required */
+} wql_status;
+
+typedef enum wql_dtype {
+  WQL_F32 = 0,   /* IEEE binary32 */
+  WQL_F16 = 1,   /* IEEE binary16 */
+  WQL_BF16 = 2   /* bfloat16 */
+} wql_dtype;
+
+typedef enum wql_clip {
+  WQL_CLIP_RTN = 0,  /* scale = amax / qmax (ratio 1.0 only) */
+  WQL_CLIP_MSE = 1   /* ratios 1.0, 0.95, 0.9, 0.85, 0.8; least squared error */
+} wql_clip;
+
+/* A quantised lm_head weight as produced by wql_quantize().
+ *   bits 4: qweight is int32 [n, k/8]; element k = 8i + j of a row is the
+ *           nibble in bits [4j, 4j + 4) of word i (least significant first);
+ *           nibble = q + 8.  (The page's in-word "ExLlama shuffle" order is
+ *           not defined there; this natural order is this library's format.)
+ *   bits 8: qweight is int8 [n, k], two's complement q in [-127, 127].
+ *   scales: [n, k / group] of scale_dtype, or [n, 1] when group == 0.
+ * Requirements: k % 64 == 0; group is 0 or a multiple of 64 dividing k;
+ * qweight 16-byte aligned; scales 2-byte aligned; n < 2^31. */
+typedef struct wql_weight {
+  int32_t bits;         /* 4 or 8 */
+  int32_t group;        /* G (multiple of 64) or 0 = one scale per row */
+  int32_t scale_dtype;  /* WQL_F16 or WQL_BF16 */
+  int32_t reserved;     /* must be 0 */
+  int64_t n;            /* vocab rows */
+  int64_t k;            /* hidden size */
+  const void* qweight;  /* device */
+  const void* scales;   /* device */
+} wql_weight;
+
+/* Largest top-K width supported by wql_logits / wql_topk_rescore. */
+#define WQL_MAX_TOPK 16
+/* Upper bound on the CTAs one wql_logits launch uses; sizes the workspace. */
+#define WQL_MAX_CTAS 1024
+
+/* Quantise and pack a dense weight (radiance_lmhead_int4.py,
+ * quantize_int4_rows; int8 per the W8 rows of the Perf evals table).
+ * Per group of G columns (group 0: the whole row), for each tried ratio r:
+ *   s_r = RN_scale_dtype(max(fl32(amax) *f32 fl32(r / qmax), 1e-8f))
+ *   q   = clamp(round_half_even(w /f32 s_r), -8 or -127, 7 or 127),
+ *         and q = 0 for the whole group when s_r rounds to zero;
+ * RTN keeps r = 1.0; MSE keeps the first ratio whose binary64 error
+ * sum_k (q*s - w)^2 (k ascending) is strictly the smallest.
+ *   w            device [n, k] of w_dtype (F32, F16 or BF16), 16-byte aligned
+ *   qweight_out  device, layout of wql_weight for `bits`
+ *   scales_out   device [n, k / group] (or [n]) of scale_dtype
+ * Results are bit-exact with the definition above. */
+wql_status wql_quantize(const void* w, int32_t w_dtype, int64_t n, int64_t k,
+                        int32_t bits, int32_t group, int32_t scale_dtype,
+                        int32_t clip, void* qweight_out, void* scales_out,
+                        cudaStream_t stream);
+
+/* Pack nibbles (uint8 [n, k], values 0..15; higher bits are ignored) into the
+ * int4 layout of wql_weight: packed_out int32 [n, k/8].  k % 8 == 0. */
+wql_status wql_pack(const uint8_t* nibbles, int64_t n, int64_t k,
+                    int32_t* packed_out, cudaStream_t stream);
+
+/* Inverse of wql_pack: nibbles_out uint8 [n, k] in 0..15.  k % 8 == 0. */
+wql_status wql_unpack(const int32_t* packed, int64_t n, int64_t k,
+                      uint8_t* nibbles_out, cudaStream_t stream);
+
+/* Bytes of workspace wql_logits needs for m token rows and top-K width topk
+ * (n is the vocab size).  Pure host arithmetic; never touches the GPU.  The
+ * buffer must be zero-filled once before its first use; every call leaves it
+ * ready for the next.  Calls that may run concurrently need separate
+ * workspaces. */
+size_t wql_workspace_size(int64_t m, int64_t n, int32_t topk);
+
+/* Logits of a quantised lm_head ("Fused WNA16 GEMM for tied quantized lm_head
+ * logits", Purpose; radiance_lmhead_int4.py, apply()).
+ *   x          device [m, k] of x_dtype (F16 or BF16), 16-byte aligned
+ *   w          quantised weight (host struct; its pointers are device)
+ *   bias       device [n] of x_dtype, or NULL
+ *   logits_out device [m, n] of x_dtype: fp32 accumulation, then rounded to
+ *              nearest-even in x_dtype
+ *   topk       0 (no candidates) or 1..WQL_MAX_TOPK, topk <= n
+ *   topk_idx   device int32 [m, topk] (NULL when topk == 0)
+ *   topk_val   device float [m, topk]: the fp32 logits before output
+ *              rounding, ordered by value descending, then index ascending
+ *   workspace  device, ws_bytes >= wql_workspace_size(m, n, topk)
+ * The kernel is chosen from m inside the library. */
+wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m,
+                      const wql_weight* w, const void* bias, void* logits_out,
+                      int32_t topk, int32_t* topk_idx, float* topk_val,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Exact top-K rescoring ("Fused WNA16 GEMM for tied quantized lm_head
+ * logits", reviewer comment item 2): for every row m and each of its topk
+ * candidate indices, recompute v = sum_k x[m,k] * w_ref[idx,k] (+ bias[idx])
+ * with fp32 accumulation of the exact products, write logits[m, idx] =
+ * RN_x_dtype(v), replace topk_val by v and re-sort the row's candidates by
+ * value descending, then index ascending.
+ *   x            device [m, k] of x_dtype (F16 or BF16)
+ *   w_ref        device [n, k] unquantised weight, dtype == x_dtype
+ *   bias         device [n] of x_dtype, or NULL
+ *   topk_idx     device int32 [m, topk], each in [0, n) (in/out)
+ *   topk_val     device float [m, topk] (in/out)
+ *   logits_inout device [m, n] of x_dtype
+ * k % 8 == 0; x and w_ref 16-byte aligned. */
+wql_status wql_topk_rescore(const void* x, int32_t x_dtype, int64_t m,
+                            const void* w_ref, int32_t wref_dtype, int64_t n,
+                            int64_t k, const void* bias, int32_t topk,
+                            int32_t* topk_idx, float* topk_val,
+                            void* logits_inout, cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* wql_status_string(wql_status status);
+
+/* Text of the last CUDA error seen by this host thread ("" if none). */
+const char* wql_last_error(void);
+
+/* Number of kernels this process has launched through the library. */
+uint64_t wql_launch_count(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* WQL_H_ */

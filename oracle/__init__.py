@@ -70,9 +70,11 @@ def _load():
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_quantize.restype = i32
-        lib.oracle_quantize.argtypes = [vp, i32, i64, i64, i32, i32, i32, i32, vp, vp, vp]
+        lib.oracle_quantize.argtypes = [vp, i32, i64, i64, i32, i32, i32, i32, vp, vp, vp, i32]
         lib.oracle_pack_int4.restype = i32
         lib.oracle_pack_int4.argtypes = [vp, i64, i64, vp]
+        lib.oracle_pack_codes_int4.restype = i32
+        lib.oracle_pack_codes_int4.argtypes = [vp, i64, i64, vp]
         lib.oracle_unpack_int4.restype = i32
         lib.oracle_unpack_int4.argtypes = [vp, i64, i64, vp]
         lib.oracle_logits.restype = i32
@@ -133,7 +135,7 @@ def scales_to_f64(bits: np.ndarray, scale_dtype: int) -> np.ndarray:
 # --- quantiser, packing ----------------------------------------------------
 
 def quantize(w: np.ndarray, w_dtype: int, bits: int, group: int, scale_dtype: int,
-             clip: int):
+             clip: int, nthreads: int = 1):
     """Returns (q int8 [n,k] signed codes, scale bits uint16 [n, k/G], ratio idx int8)."""
     lib = _load()
     n, k = w.shape
@@ -143,10 +145,23 @@ def quantize(w: np.ndarray, w_dtype: int, bits: int, group: int, scale_dtype: in
     s = np.empty((n, k // g), dtype=np.uint16)
     r = np.empty((n, k // g), dtype=np.int8)
     rc = lib.oracle_quantize(_ptr(wb), w_dtype, n, k, bits, group, scale_dtype, clip,
-                             _ptr(q), _ptr(s), _ptr(r))
+                             _ptr(q), _ptr(s), _ptr(r), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_quantize rejected its arguments")
     return q, s, r
+
+
+def quantize_packed(w: np.ndarray, w_dtype: int, bits: int, group: int, scale_dtype: int,
+                    clip: int, nthreads: int = 1):
+    """(qweight in the library layout, scale bits): int4 packed words or int8 codes."""
+    q, s, _ = quantize(w, w_dtype, bits, group, scale_dtype, clip, nthreads)
+    if bits == 4:
+        n, k = q.shape
+        out = np.empty((n, k // 8), dtype=np.uint32)
+        if _load().oracle_pack_codes_int4(_ptr(q), n, k, _ptr(out)) != 0:
+            raise ValueError("k must be a multiple of 8")
+        return out.view(np.int32), s
+    return q, s
 
 
 def pack_int4(nibbles: np.ndarray) -> np.ndarray:

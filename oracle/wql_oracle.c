@@ -151,9 +151,9 @@ static const double kClipRatios[5] = {1.0, 0.95, 0.9, 0.85, 0.8};
  * q_out: n*k signed codes.  scales_out: n*(k/group) storage-dtype bits.
  * ratio_out (nullable): index of the chosen clip ratio per group.
  * Returns 0, or -1 on bad arguments. */
-int oracle_quantize(const void* w, int w_dtype, int64_t n, int64_t k, int bits,
-                    int group, int scale_dtype, int clip, int8_t* q_out,
-                    uint16_t* scales_out, int8_t* ratio_out) {
+static int quantize_rows(const void* w, int w_dtype, int64_t row_begin, int64_t row_end,
+                         int64_t k, int bits, int group, int scale_dtype, int clip,
+                         int8_t* q_out, uint16_t* scales_out, int8_t* ratio_out) {
   if (bits != 4 && bits != 8) return -1;
   int64_t g = group == 0 ? k : group;
   if (g <= 0 || k % g != 0) return -1;
@@ -162,14 +162,17 @@ int oracle_quantize(const void* w, int w_dtype, int64_t n, int64_t k, int bits,
   const int nratios = clip ? 5 : 1;
   const int64_t ngroups = k / g;
   int8_t* qtry = (int8_t*)malloc((size_t)g);
-  if (!qtry) return -1;
-  for (int64_t row = 0; row < n; ++row) {
+  float* wbuf = (float*)malloc((size_t)g * sizeof(float));
+  if (!qtry || !wbuf) { free(qtry); free(wbuf); return -1; }
+  for (int64_t row = row_begin; row < row_end; ++row) {
     for (int64_t gi = 0; gi < ngroups; ++gi) {
       const int64_t base = row * k + gi * g;
+      /* the group's values, widened exactly to fp32 */
+      for (int64_t j = 0; j < g; ++j) wbuf[j] = (float)load_elem(w, w_dtype, base + j);
       /* amax over the group, in fp32 (exact: max of magnitudes) */
       float amax = 0.0f;
       for (int64_t j = 0; j < g; ++j) {
-        float a = fabsf((float)load_elem(w, w_dtype, base + j));
+        float a = fabsf(wbuf[j]);
         if (a > amax) amax = a;
       }
       double best_err = 0.0;
@@ -183,7 +186,7 @@ int oracle_quantize(const void* w, int w_dtype, int64_t n, int64_t k, int bits,
         float s = (float)scale_value(sbits, scale_dtype); /* exact widening */
         double err = 0.0;
         for (int64_t j = 0; j < g; ++j) {
-          float wv = (float)load_elem(w, w_dtype, base + j);
+          float wv = wbuf[j];
           int q;
           if (s == 0.0f) {
             q = 0;
@@ -212,7 +215,50 @@ int oracle_quantize(const void* w, int w_dtype, int64_t n, int64_t k, int bits,
     }
   }
   free(qtry);
+  free(wbuf);
   return 0;
+}
+
+typedef struct {
+  const void* w; int w_dtype; int64_t r0, r1, k; int bits, group, scale_dtype, clip;
+  int8_t* q_out; uint16_t* scales_out; int8_t* ratio_out; int rc;
+} quant_job;
+
+static void* quant_worker(void* arg) {
+  quant_job* J = (quant_job*)arg;
+  J->rc = quantize_rows(J->w, J->w_dtype, J->r0, J->r1, J->k, J->bits, J->group,
+                        J->scale_dtype, J->clip, J->q_out, J->scales_out, J->ratio_out);
+  return NULL;
+}
+
+/* Rows are independent; nthreads >= 1 splits them into contiguous blocks. */
+int oracle_quantize(const void* w, int w_dtype, int64_t n, int64_t k, int bits,
+                    int group, int scale_dtype, int clip, int8_t* q_out,
+                    uint16_t* scales_out, int8_t* ratio_out, int nthreads) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  int joined[256];
+  quant_job jobs[256];
+  int64_t per = (n + nthreads - 1) / nthreads;
+  for (int t = 0; t < nthreads; ++t) {
+    int64_t r0 = t * per < n ? t * per : n;
+    int64_t r1 = (t + 1) * per < n ? (t + 1) * per : n;
+    quant_job J = {w, w_dtype, r0, r1, k, bits, group, scale_dtype, clip,
+                   q_out, scales_out, ratio_out, 0};
+    jobs[t] = J;
+    joined[t] = 0;
+    if (nthreads == 1 || pthread_create(&th[t], NULL, quant_worker, &jobs[t]) != 0) {
+      quant_worker(&jobs[t]);
+      joined[t] = 1;
+    }
+  }
+  int rc = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    if (!joined[t]) pthread_join(th[t], NULL);
+    if (jobs[t].rc != 0) rc = jobs[t].rc;
+  }
+  return rc;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -226,6 +272,19 @@ int oracle_pack_int4(const uint8_t* nib, int64_t n, int64_t k, uint32_t* packed)
       uint32_t word = 0;
       for (int j = 0; j < 8; ++j)
         word |= ((uint32_t)(nib[r * k + 8 * i + j] & 15u)) << (4 * j);
+      packed[r * (k / 8) + i] = word;
+    }
+  return 0;
+}
+
+/* Pack signed int4 codes q in [-8, 7] as nibbles q + 8 (same layout). */
+int oracle_pack_codes_int4(const int8_t* q, int64_t n, int64_t k, uint32_t* packed) {
+  if (k % 8 != 0) return -1;
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t i = 0; i < k / 8; ++i) {
+      uint32_t word = 0;
+      for (int j = 0; j < 8; ++j)
+        word |= ((uint32_t)(q[r * k + 8 * i + j] + 8) & 15u) << (4 * j);
       packed[r * (k / 8) + i] = word;
     }
   return 0;
@@ -255,7 +314,9 @@ typedef struct {
   int64_t r_begin, r_end;
 } logits_job;
 
-static double dequant(const logits_job* J, int64_t row, int64_t kk) {
+/* w[row, kk] = q * s, from the packed codes (explicit nibble unpack) and the
+ * row's scales already widened to binary64 in srow. */
+static double dequant(const logits_job* J, const double* srow, int64_t row, int64_t kk) {
   int q;
   if (J->bits == 4) {
     const uint32_t* P = (const uint32_t*)J->qweight;
@@ -265,20 +326,27 @@ static double dequant(const logits_job* J, int64_t row, int64_t kk) {
   } else {
     q = (int)((const int8_t*)J->qweight)[row * J->k + kk];
   }
-  int64_t ngroups = J->k / J->group;
-  double s = scale_value(J->scales[row * ngroups + kk / J->group], J->scale_dtype);
-  return (double)q * s;
+  return (double)q * srow[kk / J->group];
 }
 
 static void* logits_worker(void* arg) {
   const logits_job* J = (const logits_job*)arg;
+  const int64_t ngroups = J->k / J->group;
+  double* xd = (double*)malloc((size_t)(J->m * J->k) * sizeof(double));
+  double* srow = (double*)malloc((size_t)ngroups * sizeof(double));
+  double* wrow = (double*)malloc((size_t)J->k * sizeof(double));
+  if (!xd || !srow || !wrow) { free(xd); free(srow); free(wrow); return (void*)1; }
+  for (int64_t i = 0; i < J->m * J->k; ++i) xd[i] = load_elem(J->x, J->x_dtype, i);
   for (int64_t ri = J->r_begin; ri < J->r_end; ++ri) {
     int64_t row = J->rows ? J->rows[ri] : ri;
+    for (int64_t gi = 0; gi < ngroups; ++gi)
+      srow[gi] = scale_value(J->scales[row * ngroups + gi], J->scale_dtype);
+    for (int64_t kk = 0; kk < J->k; ++kk) wrow[kk] = dequant(J, srow, row, kk);
     for (int64_t mi = 0; mi < J->m; ++mi) {
+      const double* xr = xd + mi * J->k;
       double acc = 0.0, absacc = 0.0;
       for (int64_t kk = 0; kk < J->k; ++kk) {
-        double xv = load_elem(J->x, J->x_dtype, mi * J->k + kk);
-        double p = xv * dequant(J, row, kk);
+        double p = xr[kk] * wrow[kk];
         acc = acc + p;
         absacc = absacc + fabs(p);
       }
@@ -287,6 +355,7 @@ static void* logits_worker(void* arg) {
       if (J->abs_out) J->abs_out[mi * J->nrows + ri] = absacc;
     }
   }
+  free(xd); free(srow); free(wrow);
   return NULL;
 }
 

@@ -1,0 +1,109 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/wql.h declares, and rejects bad arguments on the host before any CUDA
+call (so these checks run anywhere).  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_only_quantized_wql_gb300 as wql
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wql.h")
+OK, EINVAL, EUNSUPPORTED, ECUDA, EWORKSPACE = 0, 1, 2, 3, 4
+A = 0x7F0000100000  # an aligned fake device address: never dereferenced by the checks
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return wql.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wql_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("wql_quantize", "wql_pack", "wql_unpack", "wql_workspace_size",
+                     "wql_logits", "wql_topk_rescore", "wql_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libwql.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code, tag in [(OK, "WQL_OK"), (EINVAL, "WQL_EINVAL"), (EUNSUPPORTED, "WQL_EUNSUPPORTED"),
+                      (ECUDA, "WQL_ECUDA"), (EWORKSPACE, "WQL_EWORKSPACE")]:
+        assert wql.wql_status_string(code).startswith(tag)
+
+
+def test_workspace_size_arithmetic():
+    assert wql.wql_workspace_size(1, 1000, 0) == 256
+    s = wql.wql_workspace_size(3, 1000, 8)
+    assert s >= 256 + 3 * wql.MAX_CTAS * 8 * 8 + 3 * 1000 * 4 and s % 256 == 0
+    assert wql.wql_workspace_size(-1, 10, 8) == 0
+    assert wql.wql_workspace_size(1, 10, wql.MAX_TOPK + 1) == 0
+
+
+def _weight(bits=4, group=64, sdt=1, n=1000, k=512, reserved=0, q=A, s=A):
+    return wql._WqlWeight(bits, group, sdt, reserved, n, k, q, s)
+
+
+def _logits(lib, w, x=A, xdt=1, m=2, bias=None, out=A, topk=0, idx=None, val=None, ws=None,
+            wsb=0):
+    return lib.wql_logits(x, xdt, m, ctypes.byref(w) if w is not None else None, bias, out,
+                          topk, idx, val, ws, wsb, None)
+
+
+def test_logits_argument_checks(lib):
+    before = wql.wql_launch_count()
+    assert _logits(lib, None) == EINVAL
+    assert _logits(lib, _weight(), m=-1) == EINVAL
+    assert _logits(lib, _weight(reserved=1)) == EINVAL
+    assert _logits(lib, _weight(), x=None) == EINVAL
+    assert _logits(lib, _weight(q=None)) == EINVAL
+    assert _logits(lib, _weight(), topk=wql.MAX_TOPK + 1) == EINVAL
+    assert _logits(lib, _weight(n=4), topk=5, idx=A, val=A) == EINVAL
+    assert _logits(lib, _weight(), topk=8) == EINVAL            # no idx/val buffers
+    assert _logits(lib, _weight(bits=3)) == EUNSUPPORTED
+    assert _logits(lib, _weight(group=96)) == EUNSUPPORTED
+    assert _logits(lib, _weight(group=64, k=96)) == EUNSUPPORTED
+    assert _logits(lib, _weight(k=520, group=0)) == EUNSUPPORTED
+    assert _logits(lib, _weight(sdt=0)) == EUNSUPPORTED
+    assert _logits(lib, _weight(), xdt=0) == EUNSUPPORTED
+    assert _logits(lib, _weight(), x=A + 2) == EUNSUPPORTED     # x not 16-byte aligned
+    assert _logits(lib, _weight(q=A + 8)) == EUNSUPPORTED
+    assert _logits(lib, _weight(), topk=8, idx=A, val=A) == EWORKSPACE
+    need = wql.wql_workspace_size(2, 1000, 8)
+    assert _logits(lib, _weight(), topk=8, idx=A, val=A, ws=A, wsb=need - 1) == EWORKSPACE
+    assert _logits(lib, _weight(), m=0) == OK                    # empty: nothing launched
+    assert _logits(lib, _weight(n=0)) == OK
+    assert wql.wql_launch_count() == before
+
+
+def test_quantize_pack_rescore_argument_checks(lib):
+    before = wql.wql_launch_count()
+    q = lib.wql_quantize
+    assert q(A, 0, -1, 512, 4, 64, 1, 0, A, A, None) == EINVAL
+    assert q(A, 0, 10, 512, 4, 64, 1, 2, A, A, None) == EINVAL      # clip mode
+    assert q(None, 0, 10, 512, 4, 64, 1, 0, A, A, None) == EINVAL
+    assert q(A, 0, 10, 512, 3, 64, 1, 0, A, A, None) == EUNSUPPORTED
+    assert q(A, 0, 10, 512, 4, 64, 0, 0, A, A, None) == EUNSUPPORTED  # fp32 scales
+    assert q(A, 0, 10, 500, 4, 64, 1, 0, A, A, None) == EUNSUPPORTED
+    assert q(A, 0, 0, 512, 4, 64, 1, 0, A, A, None) == OK
+    assert lib.wql_pack(A, 4, 12, A, None) == EUNSUPPORTED
+    assert lib.wql_pack(None, 4, 16, A, None) == EINVAL
+    assert lib.wql_unpack(A, 0, 16, A, None) == OK
+    r = lib.wql_topk_rescore
+    assert r(A, 1, 2, A, 2, 100, 256, None, 8, A, A, A, None) == EUNSUPPORTED  # dtype mismatch
+    assert r(A, 1, 2, A, 1, 100, 252, None, 8, A, A, A, None) == EUNSUPPORTED  # k % 8
+    assert r(A, 1, 2, A, 1, 4, 256, None, 8, A, A, A, None) == EINVAL          # topk > n
+    assert r(A, 1, 2, A, 1, 100, 256, None, 0, A, A, A, None) == OK            # nothing to do
+    assert wql.wql_launch_count() == before

@@ -1,0 +1,189 @@
+"""GPU parity: libwql (through its C ABI) against the CPU oracle, small shapes.
+
+Shapes span several 16-row tiles, several CTAs and a ragged vocab tail; the
+oracle quantises the same seeded weight itself and computes binary64 logits.
+Gates: packing and quantisation bit-exact; every logit within
+1e-3 + 2e-3 * sum|x w|; top-K sets equal up to exact near-ties.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_only_quantized_wql_gb300 as wql
+from weight_only_quantized_wql_gb300 import synth
+from parity import (assert_logits_close, assert_quantized_equal, check_topk, np_bits,
+                    np_input, oracle_quantized, to_f64)
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+# (bits, group, scale dtype, weight dtype, activation dtype, clip)
+SCHEMES = [
+    (4, 64, oracle.F16, oracle.F32, oracle.F16, 0),
+    (4, 128, oracle.BF16, oracle.BF16, oracle.BF16, 1),
+    (4, 128, oracle.F16, oracle.F32, oracle.F16, 0),
+    (4, 0, oracle.F16, oracle.F16, oracle.F16, 0),
+    (8, 128, oracle.F16, oracle.F32, oracle.F16, 0),
+    (8, 0, oracle.F16, oracle.F16, oracle.F16, 0),
+    (8, 64, oracle.BF16, oracle.BF16, oracle.BF16, 1),
+]
+TORCH_OF = {oracle.F32: torch.float32, oracle.F16: torch.float16, oracle.BF16: torch.bfloat16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    torch.cuda.set_device(DEV)
+    wql.load()
+
+
+def _make(n, k, scheme, seed=0):
+    bits, group, sdt, wdt, xdt, clip = scheme
+    w = synth.weight(n, k, wdt, seed=seed)
+    qw = wql.wql_quantize(w.to(DEV), bits, group, TORCH_OF[sdt], clip)
+    o_qw, o_s = oracle_quantized(w, wdt, bits, group, sdt, clip)
+    return w, qw, o_qw, o_s
+
+
+@pytest.mark.parametrize("scheme", SCHEMES, ids=lambda s: f"w{s[0]}g{s[1]}s{s[2]}w{s[3]}c{s[5]}")
+@pytest.mark.parametrize("n,k", [(1000, 512), (77, 256), (16, 320)])
+def test_quantize_bit_exact(scheme, n, k):
+    if scheme[1] and k % scheme[1]:
+        pytest.skip("group does not divide k")
+    w, qw, o_qw, o_s = _make(n, k, scheme)
+    torch.cuda.synchronize()
+    assert_quantized_equal(qw, o_qw, o_s)
+
+
+def test_quantize_edge_values():
+    # zero rows, a single outlier, exact ties for round-half-even, fp16 underflow
+    n, k = 8, 128
+    w = torch.zeros(n, k, dtype=torch.float32)
+    w[1, 5] = 1e-9                    # scale underflows in fp16 -> codes 0
+    w[2, :] = torch.linspace(-7, 7, k)
+    w[3, :8] = torch.tensor([7.0, -7.0, 3.5, -3.5, 0.5, 1.5, 2.5, -0.5])
+    w[4, :] = 1e-30
+    w[5, 0] = 3e38
+    w[6, :] = -0.02
+    w[7, ::2] = 0.013
+    for bits, group, sdt, clip in [(4, 64, oracle.F16, 0), (4, 64, oracle.BF16, 1),
+                                   (8, 128, oracle.F16, 0), (8, 0, oracle.BF16, 1)]:
+        qw = wql.wql_quantize(w.to(DEV), bits, group, TORCH_OF[sdt], clip)
+        o_qw, o_s = oracle_quantized(w, oracle.F32, bits, group, sdt, clip)
+        torch.cuda.synchronize()
+        assert_quantized_equal(qw, o_qw, o_s)
+
+
+def test_pack_unpack_against_oracle():
+    nib = synth.random_nibbles(123, 96)
+    packed = wql.wql_pack(nib.to(DEV))
+    o = oracle.pack_int4(nib.numpy())
+    assert np.array_equal(packed.cpu().numpy(), o)
+    back = wql.wql_unpack(packed, 96)
+    assert torch.equal(back.cpu(), nib)
+
+
+@pytest.mark.parametrize("scheme", SCHEMES, ids=lambda s: f"w{s[0]}g{s[1]}s{s[2]}x{s[4]}")
+@pytest.mark.parametrize("m", [1, 2, 3, 5, 8, 9, 16, 17, 33])
+def test_logits_small(scheme, m):
+    n, k, K = 1000, 512, 8
+    bits, group, sdt, wdt, xdt, clip = scheme
+    w, qw, o_qw, o_s = _make(n, k, scheme, seed=m)
+    x = synth.activations(m, k, xdt, seed=100 + m)
+    logits, idx, val = wql.wql_logits(x.to(DEV), qw, topk=K)
+    torch.cuda.synchronize()
+    ref, absacc = oracle.logits(np_input(x, xdt), xdt, o_qw, bits, o_s, sdt, group, n, k,
+                                nthreads=4)
+    assert_logits_close(to_f64(logits), ref, absacc, f"m={m}")
+    g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
+    ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K) for r in range(m))
+    assert ties <= max(1, m // 8)
+
+
+@pytest.mark.parametrize("n", [9, 16, 17, 31, 4099])
+def test_logits_ragged_vocab_and_bias(n):
+    k, m = 256, 4
+    scheme = SCHEMES[0]
+    bits, group, sdt, wdt, xdt, clip = scheme
+    w, qw, o_qw, o_s = _make(n, k, scheme, seed=n)
+    x = synth.activations(m, k, xdt, seed=7)
+    b = synth.bias(n, xdt)
+    K = min(8, n)
+    logits, idx, val = wql.wql_logits(x.to(DEV), qw, bias=b.to(DEV), topk=K)
+    torch.cuda.synchronize()
+    ref, absacc = oracle.logits(np_input(x, xdt), xdt, o_qw, bits, o_s, sdt, group, n, k,
+                                bias=np_bits(b))
+    assert_logits_close(to_f64(logits), ref, absacc, f"n={n}")
+    for r in range(m):
+        check_topk(idx.cpu().numpy()[r], val.cpu().numpy()[r], ref[r], absacc[r], K)
+
+
+def test_logits_without_topk_and_leading_shape():
+    n, k = 600, 256
+    w, qw, o_qw, o_s = _make(n, k, SCHEMES[4])
+    x = synth.activations(6, k, oracle.F16, seed=3).reshape(2, 3, k)
+    logits, idx, val = wql.wql_logits(x.to(DEV), qw, topk=0)
+    torch.cuda.synchronize()
+    assert logits.shape == (2, 3, n) and idx is None
+    ref, absacc = oracle.logits(np_input(x.reshape(6, k), oracle.F16), oracle.F16, o_qw, 8, o_s,
+                                oracle.F16, 128, n, k)
+    assert_logits_close(to_f64(logits.reshape(6, n)), ref, absacc)
+
+
+@pytest.mark.parametrize("xdt", [oracle.F16, oracle.BF16])
+def test_topk_rescore(xdt):
+    n, k, m, K = 3000, 512, 5, 8
+    scheme = (8, 0, oracle.F16 if xdt == oracle.F16 else oracle.BF16, xdt, xdt, 0)
+    bits, group, sdt, wdt, _, clip = scheme
+    w, qw, o_qw, o_s = _make(n, k, scheme)
+    x = synth.activations(m, k, xdt, seed=11)
+    b = synth.bias(n, xdt)
+    xd, wd, bd = x.to(DEV), w.to(DEV), b.to(DEV)
+    logits, idx, val = wql.wql_logits(xd, qw, bias=bd, topk=K)
+    before = logits.clone()
+    wql.wql_topk_rescore(xd, wd, idx, val, logits, bias=bd)
+    torch.cuda.synchronize()
+    g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
+    o_val, o_abs = oracle.rescore(np_input(x, xdt), xdt, np_input(w, wdt), wdt, g_idx,
+                                  bias=np_bits(b))
+    assert np.all(np.abs(g_val - o_val) <= oracle.tolerance(o_abs))
+    for r in range(m):
+        assert np.all(np.diff(g_val[r]) <= 0)
+        # rescored entries are scattered into the logits; the rest are untouched
+        row = logits[r].cpu()
+        ref_row = torch.tensor(g_val[r]).to(logits.dtype)
+        assert torch.equal(row[torch.tensor(g_idx[r], dtype=torch.long)], ref_row)
+        mask = torch.ones(n, dtype=torch.bool)
+        mask[torch.tensor(g_idx[r], dtype=torch.long)] = False
+        assert torch.equal(row[mask], before[r].cpu()[mask])
+
+
+def test_empty_and_errors():
+    n, k = 100, 256
+    w, qw, o_qw, o_s = _make(n, k, SCHEMES[0])
+    x = torch.empty(0, k, dtype=torch.float16, device=DEV)
+    logits, _, _ = wql.wql_logits(x, qw, topk=0)
+    assert logits.shape == (0, n)
+    xx = synth.activations(2, k, oracle.F16).to(DEV)
+    with pytest.raises(wql.WQLError):
+        wql.wql_logits(xx, qw, topk=n + 1)
+    with pytest.raises(wql.WQLError):
+        wql.wql_logits(xx, qw, topk=wql.MAX_TOPK + 1)
+    bad = wql.QuantizedWeight(qw.qweight, qw.scales, 4, 64, n, 200)
+    with pytest.raises(wql.WQLError):
+        wql.wql_logits(synth.activations(2, 200, oracle.F16).to(DEV), bad)
+
+
+def test_workspace_reuse_across_calls():
+    # the per-call ticket counter must be left at zero for the next call
+    n, k = 5000, 256
+    w, qw, o_qw, o_s = _make(n, k, SCHEMES[0])
+    ws = wql.Workspace(DEV)
+    x = synth.activations(3, k, oracle.F16, seed=5)
+    ref, absacc = oracle.logits(np_input(x, oracle.F16), oracle.F16, o_qw, 4, o_s, oracle.F16,
+                                64, n, k)
+    for _ in range(5):
+        logits, idx, val = wql.wql_logits(x.to(DEV), qw, topk=8, workspace=ws)
+        torch.cuda.synchronize()
+        for r in range(3):
+            check_topk(idx.cpu().numpy()[r], val.cpu().numpy()[r], ref[r], absacc[r], 8)

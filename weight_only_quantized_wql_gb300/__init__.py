@@ -1,0 +1,267 @@
+"""Weight-only quantised lm_head logits on GB300 -- Python binding of libwql.
+
+Thin ctypes wrappers with the C ABI's names (``include/wql.h``).  They only
+marshal arguments: torch tensors supply device memory and the current CUDA
+stream, and every step of the computation runs in libwql's CUDA kernels.
+There is no CPU or PyTorch fallback: if the library cannot be loaded, or a
+tensor is not on a CUDA device, the call raises.
+
+Functions
+  wql_quantize(w, bits, group, scale_dtype, clip)   -> QuantizedWeight
+  wql_pack(nibbles) / wql_unpack(packed, k)
+  wql_workspace_size(m, n, topk)                    -> bytes
+  wql_logits(x, qw, bias=None, topk=0, workspace=None, out=None)
+                                                    -> (logits, topk_idx, topk_val)
+  wql_topk_rescore(x, w_ref, topk_idx, topk_val, logits, bias=None)
+  wql_status_string, wql_last_error, wql_launch_count
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "WQLError", "QuantizedWeight", "Workspace", "load", "wql_quantize", "wql_pack",
+    "wql_unpack", "wql_workspace_size", "wql_logits", "wql_topk_rescore",
+    "wql_status_string", "wql_last_error", "wql_launch_count", "F32", "F16", "BF16",
+    "CLIP_RTN", "CLIP_MSE", "MAX_TOPK",
+]
+
+F32, F16, BF16 = 0, 1, 2
+CLIP_RTN, CLIP_MSE = 0, 1
+MAX_TOPK = 16
+MAX_CTAS = 1024
+_DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+_CODE_DTYPE = {v: k for k, v in _DTYPE_CODE.items()}
+_STATUS = {0: "WQL_OK", 1: "WQL_EINVAL", 2: "WQL_EUNSUPPORTED", 3: "WQL_ECUDA",
+           4: "WQL_EWORKSPACE"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class WQLError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = f"{fn} failed: {_STATUS.get(status, status)}"
+        if status == 3 and _lib is not None:
+            msg += f" ({_lib.wql_last_error().decode()})"
+        super().__init__(msg)
+
+
+class _WqlWeight(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("scale_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libwql.so (building it first when it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libwql.so not found at {path}; run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        i32, i64, vp, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+        lib.wql_quantize.restype = i32
+        lib.wql_quantize.argtypes = [vp, i32, i64, i64, i32, i32, i32, i32, vp, vp, vp]
+        lib.wql_pack.restype = i32
+        lib.wql_pack.argtypes = [vp, i64, i64, vp, vp]
+        lib.wql_unpack.restype = i32
+        lib.wql_unpack.argtypes = [vp, i64, i64, vp, vp]
+        lib.wql_workspace_size.restype = sz
+        lib.wql_workspace_size.argtypes = [i64, i64, i32]
+        lib.wql_logits.restype = i32
+        lib.wql_logits.argtypes = [vp, i32, i64, ctypes.POINTER(_WqlWeight), vp, vp, i32, vp,
+                                   vp, vp, sz, vp]
+        lib.wql_topk_rescore.restype = i32
+        lib.wql_topk_rescore.argtypes = [vp, i32, i64, vp, i32, i64, i64, vp, i32, vp, vp, vp,
+                                         vp]
+        lib.wql_status_string.restype = ctypes.c_char_p
+        lib.wql_status_string.argtypes = [i32]
+        lib.wql_last_error.restype = ctypes.c_char_p
+        lib.wql_last_error.argtypes = []
+        lib.wql_launch_count.restype = ctypes.c_uint64
+        lib.wql_launch_count.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise WQLError(fn, status)
+
+
+def _cuda(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+@dataclass
+class QuantizedWeight:
+    """Packed weight + scale table, in the layout wql.h documents."""
+    qweight: torch.Tensor      # int32 [n, k/8] (bits 4) or int8 [n, k] (bits 8)
+    scales: torch.Tensor       # fp16/bf16 [n, k/group] (or [n, 1])
+    bits: int
+    group: int                 # 0 = one scale per row
+    n: int
+    k: int
+
+    @property
+    def scale_dtype(self) -> int:
+        return _DTYPE_CODE[self.scales.dtype]
+
+    def _struct(self) -> _WqlWeight:
+        return _WqlWeight(self.bits, self.group, self.scale_dtype, 0, self.n, self.k,
+                          self.qweight.data_ptr(), self.scales.data_ptr())
+
+    def nbytes(self) -> int:
+        return self.qweight.numel() * self.qweight.element_size() + \
+            self.scales.numel() * self.scales.element_size()
+
+
+class Workspace:
+    """Zero-initialised device scratch for wql_logits, grown on demand."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws: dict = {}
+
+
+def wql_status_string(status: int) -> str:
+    return load().wql_status_string(status).decode()
+
+
+def wql_last_error() -> str:
+    return load().wql_last_error().decode()
+
+
+def wql_launch_count() -> int:
+    return int(load().wql_launch_count())
+
+
+def wql_workspace_size(m: int, n: int, topk: int) -> int:
+    return int(load().wql_workspace_size(m, n, topk))
+
+
+def wql_quantize(w: torch.Tensor, bits: int, group: int, scale_dtype=torch.float16,
+                 clip: int = CLIP_RTN) -> QuantizedWeight:
+    """Quantise + pack a [n, k] fp32/fp16/bf16 CUDA weight (see wql.h)."""
+    lib = load()
+    _cuda(w, "w")
+    n, k = w.shape
+    g = k if group == 0 else group
+    if bits == 4:
+        qw = torch.empty((n, k // 8), dtype=torch.int32, device=w.device)
+    else:
+        qw = torch.empty((n, k), dtype=torch.int8, device=w.device)
+    sc = torch.empty((n, k // g if g else 0), dtype=scale_dtype, device=w.device)
+    _check("wql_quantize", lib.wql_quantize(_ptr(w), _DTYPE_CODE[w.dtype], n, k, bits, group,
+                                            _DTYPE_CODE[scale_dtype], clip, _ptr(qw),
+                                            _ptr(sc), _stream(w.device)))
+    return QuantizedWeight(qw, sc, bits, group, n, k)
+
+
+def wql_pack(nibbles: torch.Tensor) -> torch.Tensor:
+    lib = load()
+    _cuda(nibbles, "nibbles")
+    n, k = nibbles.shape
+    out = torch.empty((n, k // 8), dtype=torch.int32, device=nibbles.device)
+    _check("wql_pack", lib.wql_pack(_ptr(nibbles), n, k, _ptr(out), _stream(nibbles.device)))
+    return out
+
+
+def wql_unpack(packed: torch.Tensor, k: int) -> torch.Tensor:
+    lib = load()
+    _cuda(packed, "packed")
+    n = packed.shape[0]
+    out = torch.empty((n, k), dtype=torch.uint8, device=packed.device)
+    _check("wql_unpack", lib.wql_unpack(_ptr(packed), n, k, _ptr(out), _stream(packed.device)))
+    return out
+
+
+def wql_logits(x: torch.Tensor, qw: QuantizedWeight, bias: torch.Tensor | None = None,
+               topk: int = 0, workspace: Workspace | None = None,
+               out: torch.Tensor | None = None, topk_idx: torch.Tensor | None = None,
+               topk_val: torch.Tensor | None = None):
+    """logits [m, n] (x.dtype), and top-K (idx int32, val fp32) when topk > 0.
+
+    x of any leading shape is flattened to [m, k] (radiance_lmhead_int4.py,
+    apply()); the logits are returned with x's leading shape."""
+    lib = load()
+    lead = x.shape[:-1]
+    x2 = x.reshape(-1, x.shape[-1])
+    _cuda(x2, "x")
+    m = x2.shape[0]
+    if out is None:
+        out = torch.empty((m, qw.n), dtype=x.dtype, device=x.device)
+    if topk > 0:
+        if topk_idx is None:
+            topk_idx = torch.empty((m, topk), dtype=torch.int32, device=x.device)
+        if topk_val is None:
+            topk_val = torch.empty((m, topk), dtype=torch.float32, device=x.device)
+    need = wql_workspace_size(m, qw.n, topk)
+    if workspace is None:
+        workspace = _default_ws.setdefault((x.device, torch.cuda.current_stream(x.device)),
+                                           Workspace(x.device))
+    ws = workspace.get(need)
+    st = qw._struct()
+    _check("wql_logits", lib.wql_logits(
+        _ptr(x2), _DTYPE_CODE[x.dtype], m, ctypes.byref(st), _ptr(bias), _ptr(out), topk,
+        _ptr(topk_idx) if topk > 0 else None, _ptr(topk_val) if topk > 0 else None,
+        _ptr(ws), ws.numel(), _stream(x.device)))
+    logits = out.reshape(*lead, qw.n)
+    if topk > 0:
+        return logits, topk_idx.reshape(*lead, topk), topk_val.reshape(*lead, topk)
+    return logits, None, None
+
+
+def wql_topk_rescore(x: torch.Tensor, w_ref: torch.Tensor, topk_idx: torch.Tensor,
+                     topk_val: torch.Tensor, logits: torch.Tensor,
+                     bias: torch.Tensor | None = None) -> None:
+    """In place: exact rescoring of the top-K candidates (see wql.h)."""
+    lib = load()
+    x2 = x.reshape(-1, x.shape[-1])
+    for t, name in ((x2, "x"), (w_ref, "w_ref"), (topk_idx, "topk_idx"),
+                    (topk_val, "topk_val"), (logits, "logits")):
+        _cuda(t, name)
+    m, k = x2.shape
+    n = w_ref.shape[0]
+    topk = topk_idx.shape[-1]
+    _check("wql_topk_rescore", lib.wql_topk_rescore(
+        _ptr(x2), _DTYPE_CODE[x.dtype], m, _ptr(w_ref), _DTYPE_CODE[w_ref.dtype], n, k,
+        _ptr(bias), topk, _ptr(topk_idx), _ptr(topk_val), _ptr(logits), _stream(x.device)))

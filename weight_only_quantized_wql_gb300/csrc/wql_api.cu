@@ -1,0 +1,235 @@
+// wql_api.cu -- the extern "C" entry points declared in include/wql.h.
+//
+// Every entry point validates its arguments on the host before it touches
+// the CUDA runtime, so bad arguments never launch anything and never need a
+// GPU to be diagnosed.  Kernel choice by token count lives here.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <string>
+
+#include "wql_common.cuh"
+
+namespace wql {
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+thread_local std::string g_last_error;
+constexpr int kDecodeMaxTokens = 16;
+constexpr size_t kDecodeSmemBudget = 200 * 1024;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool half_dtype(int d) { return d == WQL_F16 || d == WQL_BF16; }
+
+wql_status cuda_fail(cudaError_t e) {
+  g_last_error = cudaGetErrorString(e);
+  return WQL_ECUDA;
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int device_sm_count() {
+  static thread_local int cached_dev = -1;
+  static thread_local int cached_sms = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev != cached_dev) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      sms = 1;
+    cached_dev = dev;
+    cached_sms = sms;
+  }
+  return cached_sms;
+}
+
+WorkspaceLayout workspace_layout(int64_t m, int64_t n, int32_t topk) {
+  WorkspaceLayout l{};
+  l.counter_off = 0;
+  size_t off = 256;
+  l.cand_off = off;
+  if (topk > 0) off += round_up((size_t)m * WQL_MAX_CTAS * (size_t)topk * 8, 256);
+  l.scratch_off = off;
+  if (topk > 0) off += round_up((size_t)m * (size_t)n * 4, 256);
+  l.total = off;
+  return l;
+}
+
+}  // namespace wql
+
+using namespace wql;
+
+extern "C" {
+
+const char* wql_status_string(wql_status status) {
+  switch (status) {
+    case WQL_OK: return "WQL_OK: success";
+    case WQL_EINVAL: return "WQL_EINVAL: invalid argument";
+    case WQL_EUNSUPPORTED: return "WQL_EUNSUPPORTED: unsupported configuration";
+    case WQL_ECUDA: return "WQL_ECUDA: CUDA error";
+    case WQL_EWORKSPACE: return "WQL_EWORKSPACE: workspace missing or too small";
+  }
+  return "unknown wql_status";
+}
+
+const char* wql_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t wql_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t wql_workspace_size(int64_t m, int64_t n, int32_t topk) {
+  if (m < 0 || n < 0 || topk < 0 || topk > WQL_MAX_TOPK) return 0;
+  return workspace_layout(m, n, topk).total;
+}
+
+wql_status wql_quantize(const void* w, int32_t w_dtype, int64_t n, int64_t k, int32_t bits,
+                        int32_t group, int32_t scale_dtype, int32_t clip, void* qweight_out,
+                        void* scales_out, cudaStream_t stream) {
+  if (n < 0 || k <= 0 || group < 0) return WQL_EINVAL;
+  if (n > 0 && (!w || !qweight_out || !scales_out)) return WQL_EINVAL;
+  if (clip != WQL_CLIP_RTN && clip != WQL_CLIP_MSE) return WQL_EINVAL;
+  if (bits != 4 && bits != 8) return WQL_EUNSUPPORTED;
+  if (w_dtype != WQL_F32 && !half_dtype(w_dtype)) return WQL_EUNSUPPORTED;
+  if (!half_dtype(scale_dtype)) return WQL_EUNSUPPORTED;
+  const int64_t g = group == 0 ? k : group;
+  if (k % 8 != 0 || k % g != 0 || g % 8 != 0) return WQL_EUNSUPPORTED;
+  if (!aligned(w, 16) || !aligned(qweight_out, 16) || !aligned(scales_out, 2))
+    return WQL_EUNSUPPORTED;
+  if (n == 0) return WQL_OK;
+  if (g > (1 << 30)) return WQL_EUNSUPPORTED;
+  QuantizeArgs a{};
+  a.w = w;
+  a.w_dtype = w_dtype;
+  a.n = n;
+  a.k = k;
+  a.bits = bits;
+  a.group_eff = (int)g;
+  a.scale_dtype = scale_dtype;
+  a.nratios = clip == WQL_CLIP_MSE ? 5 : 1;
+  static const double kRatios[5] = {1.0, 0.95, 0.9, 0.85, 0.8};
+  const double qmax = bits == 4 ? 7.0 : 127.0;
+  for (int i = 0; i < 5; ++i) a.ratio_c[i] = (float)(kRatios[i] / qmax);
+  a.qweight = qweight_out;
+  a.scales = static_cast<uint16_t*>(scales_out);
+  cudaError_t e = launch_quantize(a, stream);
+  return e == cudaSuccess ? WQL_OK : cuda_fail(e);
+}
+
+wql_status wql_pack(const uint8_t* nibbles, int64_t n, int64_t k, int32_t* packed_out,
+                    cudaStream_t stream) {
+  if (n < 0 || k < 0) return WQL_EINVAL;
+  if (n > 0 && k > 0 && (!nibbles || !packed_out)) return WQL_EINVAL;
+  if (k % 8 != 0) return WQL_EUNSUPPORTED;
+  if (!aligned(nibbles, 8) || !aligned(packed_out, 4)) return WQL_EUNSUPPORTED;
+  if (n == 0 || k == 0) return WQL_OK;
+  cudaError_t e = launch_pack(nibbles, n, k, reinterpret_cast<uint32_t*>(packed_out), stream);
+  return e == cudaSuccess ? WQL_OK : cuda_fail(e);
+}
+
+wql_status wql_unpack(const int32_t* packed, int64_t n, int64_t k, uint8_t* nibbles_out,
+                      cudaStream_t stream) {
+  if (n < 0 || k < 0) return WQL_EINVAL;
+  if (n > 0 && k > 0 && (!packed || !nibbles_out)) return WQL_EINVAL;
+  if (k % 8 != 0) return WQL_EUNSUPPORTED;
+  if (!aligned(packed, 4) || !aligned(nibbles_out, 8)) return WQL_EUNSUPPORTED;
+  if (n == 0 || k == 0) return WQL_OK;
+  cudaError_t e = launch_unpack(reinterpret_cast<const uint32_t*>(packed), n, k, nibbles_out,
+                                stream);
+  return e == cudaSuccess ? WQL_OK : cuda_fail(e);
+}
+
+wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weight* w,
+                      const void* bias, void* logits_out, int32_t topk, int32_t* topk_idx,
+                      float* topk_val, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!w || m < 0 || w->n < 0 || w->k <= 0 || w->group < 0 || w->reserved != 0)
+    return WQL_EINVAL;
+  if (topk < 0 || topk > WQL_MAX_TOPK) return WQL_EINVAL;
+  const int64_t n = w->n, k = w->k;
+  if (m > 0 && n > 0) {
+    if (!x || !w->qweight || !w->scales || !logits_out) return WQL_EINVAL;
+    if (topk > 0 && (!topk_idx || !topk_val)) return WQL_EINVAL;
+    if (topk > n) return WQL_EINVAL;
+  }
+  if (w->bits != 4 && w->bits != 8) return WQL_EUNSUPPORTED;
+  if (!half_dtype(x_dtype) || !half_dtype(w->scale_dtype)) return WQL_EUNSUPPORTED;
+  const int64_t g = w->group == 0 ? k : w->group;
+  if (k % 64 != 0 || g % 64 != 0 || k % g != 0) return WQL_EUNSUPPORTED;
+  if (n >= (int64_t(1) << 31) || m >= (int64_t(1) << 31) || k >= (int64_t(1) << 30))
+    return WQL_EUNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(w->qweight, 16) || !aligned(w->scales, 2) ||
+      !aligned(logits_out, 2) || !aligned(bias, 2))
+    return WQL_EUNSUPPORTED;
+  if (m == 0 || n == 0) return WQL_OK;
+  const WorkspaceLayout lay = workspace_layout(m, n, topk);
+  if (topk > 0 && (!workspace || ws_bytes < lay.total || !aligned(workspace, 256)))
+    return WQL_EWORKSPACE;
+  const int esz = 2;
+  // tokens per decode launch: the activations of one launch are staged in
+  // shared memory
+  int64_t chunk = kDecodeMaxTokens;
+  while (chunk > 1 && (size_t)chunk * (size_t)k * esz > kDecodeSmemBudget) --chunk;
+  if ((size_t)k * esz > kDecodeSmemBudget) return WQL_EUNSUPPORTED;
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  for (int64_t m0 = 0; m0 < m; m0 += chunk) {
+    const int64_t mc = (m - m0) < chunk ? (m - m0) : chunk;
+    LogitsArgs a{};
+    a.x = static_cast<const unsigned char*>(x) + (size_t)m0 * k * esz;
+    a.x_dtype = x_dtype;
+    a.m = (int)mc;
+    a.qweight = w->qweight;
+    a.scales = static_cast<const uint16_t*>(w->scales);
+    a.bits = w->bits;
+    a.group_eff = (int)g;
+    a.scale_dtype = w->scale_dtype;
+    a.n = (int)n;
+    a.k = (int)k;
+    a.bias = bias;
+    a.logits = static_cast<unsigned char*>(logits_out) + (size_t)m0 * n * esz;
+    a.topk = topk;
+    if (topk > 0) {
+      a.topk_idx = topk_idx + (size_t)m0 * topk;
+      a.topk_val = topk_val + (size_t)m0 * topk;
+      a.counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
+      a.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
+      a.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
+    }
+    cudaError_t e = launch_decode(a, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return WQL_OK;
+}
+
+wql_status wql_topk_rescore(const void* x, int32_t x_dtype, int64_t m, const void* w_ref,
+                            int32_t wref_dtype, int64_t n, int64_t k, const void* bias,
+                            int32_t topk, int32_t* topk_idx, float* topk_val,
+                            void* logits_inout, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k <= 0) return WQL_EINVAL;
+  if (topk < 0 || topk > WQL_MAX_TOPK || topk > n) return WQL_EINVAL;
+  if (m > 0 && topk > 0 && (!x || !w_ref || !topk_idx || !topk_val || !logits_inout))
+    return WQL_EINVAL;
+  if (!half_dtype(x_dtype) || wref_dtype != x_dtype) return WQL_EUNSUPPORTED;
+  if (k % 8 != 0) return WQL_EUNSUPPORTED;
+  if (n >= (int64_t(1) << 31) || m >= (int64_t(1) << 31)) return WQL_EUNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(w_ref, 16) || !aligned(logits_inout, 2) || !aligned(bias, 2))
+    return WQL_EUNSUPPORTED;
+  if (m == 0 || n == 0 || topk == 0) return WQL_OK;
+  RescoreArgs a{};
+  a.x = x;
+  a.x_dtype = x_dtype;
+  a.m = (int)m;
+  a.n = (int)n;
+  a.k = (int)k;
+  a.w_ref = w_ref;
+  a.bias = bias;
+  a.topk = topk;
+  a.topk_idx = topk_idx;
+  a.topk_val = topk_val;
+  a.logits = logits_inout;
+  cudaError_t e = launch_rescore(a, stream);
+  return e == cudaSuccess ? WQL_OK : cuda_fail(e);
+}
+
+}  // extern "C"

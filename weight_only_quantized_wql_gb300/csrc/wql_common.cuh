@@ -1,0 +1,331 @@
+// wql_common.cuh -- device helpers and internal launcher declarations shared
+// by the libwql CUDA sources (sm_103a).  Nothing here is part of the C ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "wql.h"
+
+namespace wql {
+
+// ---------------------------------------------------------------------------
+// Host-side bookkeeping
+// ---------------------------------------------------------------------------
+void note_launch();                 // one kernel launched through the library
+int device_sm_count();              // SMs of the current device (cached)
+
+// ---------------------------------------------------------------------------
+// Element access
+// ---------------------------------------------------------------------------
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// Scale table entries are raw 16-bit patterns; `sdt` says how to read them.
+__device__ __forceinline__ float scale_to_f32(uint16_t bits, int sdt) {
+  return sdt == WQL_F16 ? __half2float(__ushort_as_half(bits))
+                        : __bfloat162float(__ushort_as_bfloat16(bits));
+}
+
+__device__ __forceinline__ uint16_t ldg_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ldg_stream_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ldg_stream_u2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Integer code -> 16-bit float pairs without int->float converts.
+//
+// A 16-bit float whose exponent field says [1024, 2048) (fp16, pattern 0x64xx)
+// or [128, 256) (bf16, pattern 0x43xx) has unit spacing, so OR-ing a small
+// unsigned integer u into its low mantissa bits yields exactly 1024 + u (or
+// 128 + u); one packed subtract then gives the signed code exactly.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
+  uint32_t d;
+  // (a & b) | c  ->  lookup table 0xEA
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(magic));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t bfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// One 32-bit word of eight nibbles (element j in bits 4j..4j+3) -> four
+// packed pairs of exact codes q = nibble - 8:
+//   out[j] = (q[j], q[j + 4]) for j = 0..3  (low half = first element).
+template <typename XT> struct Int4Dequant;
+
+template <> struct Int4Dequant<__half> {
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t out[4]) {
+    const uint32_t kMagic = 0x64006400u;      // (1024, 1024)
+    const uint32_t kSub = 0x64086408u;        // (1032, 1032)
+    const uint32_t kOneSixteenth = 0x2C002C00u; // (1/16, 1/16)
+    const uint32_t kNeg72 = 0xD480D480u;      // (-72, -72)
+    uint32_t hi = w >> 8;
+    // nibbles in bits 0..3 of each half: 1024 + u; in bits 4..7: 1024 + 16u,
+    // which x/16 - 72 turns into u - 8.
+    out[0] = hsub2_u32(lop3_and_or(w, 0x000F000Fu, kMagic), kSub);
+    out[1] = hfma2_u32(lop3_and_or(w, 0x00F000F0u, kMagic), kOneSixteenth, kNeg72);
+    out[2] = hsub2_u32(lop3_and_or(hi, 0x000F000Fu, kMagic), kSub);
+    out[3] = hfma2_u32(lop3_and_or(hi, 0x00F000F0u, kMagic), kOneSixteenth, kNeg72);
+  }
+};
+
+template <> struct Int4Dequant<__nv_bfloat16> {
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t out[4]) {
+    const uint32_t kMagic = 0x43004300u;      // (128, 128)
+    const uint32_t kOne = 0x3F803F80u;        // (1, 1)
+    const uint32_t kNeg136 = 0xC308C308u;     // (-136, -136)
+    out[0] = bfma2_u32(lop3_and_or(w, 0x000F000Fu, kMagic), kOne, kNeg136);
+    out[1] = bfma2_u32(lop3_and_or(w >> 4, 0x000F000Fu, kMagic), kOne, kNeg136);
+    out[2] = bfma2_u32(lop3_and_or(w >> 8, 0x000F000Fu, kMagic), kOne, kNeg136);
+    out[3] = bfma2_u32(lop3_and_or(w >> 12, 0x000F000Fu, kMagic), kOne, kNeg136);
+  }
+};
+
+// One 32-bit word of four int8 codes (element j in byte j) -> two packed
+// pairs in natural order: out[0] = (q0, q1), out[1] = (q2, q3).
+template <typename XT> struct Int8Dequant;
+
+template <> struct Int8Dequant<__half> {
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t out[2]) {
+    const uint32_t b = w ^ 0x80808080u;       // byte = q + 128 in [1, 255]
+    const uint32_t kSub = 0x64806480u;        // (1152, 1152) = 1024 + 128
+    out[0] = hsub2_u32(prmt(b, 0x64646464u, 0x4140u), kSub);
+    out[1] = hsub2_u32(prmt(b, 0x64646464u, 0x4342u), kSub);
+  }
+};
+
+template <> struct Int8Dequant<__nv_bfloat16> {
+  // bf16 has no unit-spaced binade wide enough for 8-bit codes: go through
+  // the fp32 pattern 0x4B0000xx = 2^23 + byte, then pack (exact for |q|<=127).
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t out[2]) {
+    const uint32_t b = w ^ 0x80808080u;
+    const float kOff = 8388736.0f;            // 2^23 + 128
+    float f0 = __uint_as_float(prmt(b, 0x4B000000u, 0x7440u)) - kOff;
+    float f1 = __uint_as_float(prmt(b, 0x4B000000u, 0x7441u)) - kOff;
+    float f2 = __uint_as_float(prmt(b, 0x4B000000u, 0x7442u)) - kOff;
+    float f3 = __uint_as_float(prmt(b, 0x4B000000u, 0x7443u)) - kOff;
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(f0, f1);
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(f2, f3);
+    out[0] = *reinterpret_cast<uint32_t*>(&p0);
+    out[1] = *reinterpret_cast<uint32_t*>(&p1);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core MMA (m16n8k16, fp32 accumulate)
+// ---------------------------------------------------------------------------
+template <typename XT> struct Mma16816;
+
+template <> struct Mma16816<__half> {
+  static __device__ __forceinline__ void run(float d[4], const uint32_t a[4], uint32_t b0,
+                                             uint32_t b1, const float c[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]),
+          "f"(c[1]), "f"(c[2]), "f"(c[3]));
+  }
+};
+
+template <> struct Mma16816<__nv_bfloat16> {
+  static __device__ __forceinline__ void run(float d[4], const uint32_t a[4], uint32_t b0,
+                                             uint32_t b1, const float c[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]),
+          "f"(c[1]), "f"(c[2]), "f"(c[3]));
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Top-K keys: one 64-bit integer per (value, index) so that a larger key
+// ranks higher -- value descending, then index ascending.  -0 counts as +0
+// and NaN ranks below everything.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long topk_key(float v, uint32_t idx) {
+  uint32_t o;
+  if (v != v) {
+    o = 0u;
+  } else {
+    uint32_t b = __float_as_uint(v + 0.0f);
+    o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  return ((unsigned long long)o << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+__device__ __forceinline__ float key_value(unsigned long long key) {
+  uint32_t o = (uint32_t)(key >> 32);
+  uint32_t b = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+  return __uint_as_float(b);
+}
+__device__ __forceinline__ int32_t key_index(unsigned long long key) {
+  return (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+}
+constexpr unsigned long long kEmptyKey = 0ull;   // ranks below every real entry
+
+// Insert `key` into a descending register list of K entries (static indexing).
+template <int K>
+__device__ __forceinline__ void list_insert(unsigned long long (&list)[K], unsigned long long key) {
+  if (key <= list[K - 1]) return;
+#pragma unroll
+  for (int i = K - 1; i > 0; --i) {
+    unsigned long long prev = list[i - 1];
+    bool shift = key > prev;
+    list[i] = shift ? prev : (key > list[i] ? key : list[i]);
+  }
+  if (key > list[0]) list[0] = key;
+}
+
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
+  uint32_t lo = (uint32_t)v, hi = (uint32_t)(v >> 32);
+  lo = __shfl_xor_sync(0xFFFFFFFFu, lo, m);
+  hi = __shfl_xor_sync(0xFFFFFFFFu, hi, m);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) {
+    unsigned long long o = shfl_xor_u64(v, m);
+    v = o > v ? o : v;
+  }
+  return v;
+}
+
+// Merge the 32 lanes' descending lists into the warp's top `kk` keys (kk <=
+// K), returned in descending order in `out` on every lane.  Keys are unique.
+template <int K>
+__device__ __forceinline__ void warp_merge_topk(unsigned long long (&list)[K], int kk,
+                                                unsigned long long (&out)[K]) {
+#pragma unroll
+  for (int r = 0; r < K; ++r) {
+    if (r < kk) {
+      unsigned long long best = warp_max_u64(list[0]);
+      out[r] = best;
+      if (list[0] == best && best != kEmptyKey) {
+#pragma unroll
+        for (int i = 0; i < K - 1; ++i) list[i] = list[i + 1];
+        list[K - 1] = kEmptyKey;
+      }
+    } else {
+      out[r] = kEmptyKey;
+    }
+  }
+}
+
+// best[lane] without dynamic register indexing (which would go to local memory)
+template <int K>
+__device__ __forceinline__ unsigned long long pick(const unsigned long long (&v)[K], int i) {
+  unsigned long long r = kEmptyKey;
+#pragma unroll
+  for (int j = 0; j < K; ++j) r = (j == i) ? v[j] : r;
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Internal launchers
+// ---------------------------------------------------------------------------
+struct QuantizeArgs {
+  const void* w;
+  int w_dtype;
+  int64_t n, k;
+  int bits, group_eff, scale_dtype, nratios;
+  float ratio_c[5];          // fl32(r / qmax), computed on the host in binary64
+  void* qweight;
+  uint16_t* scales;
+};
+cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
+cudaError_t launch_pack(const uint8_t* nib, int64_t n, int64_t k, uint32_t* out, cudaStream_t s);
+cudaError_t launch_unpack(const uint32_t* packed, int64_t n, int64_t k, uint8_t* out,
+                          cudaStream_t s);
+
+struct LogitsArgs {
+  const void* x;
+  int x_dtype;
+  int m;                      // token rows in this launch
+  const void* qweight;
+  const uint16_t* scales;
+  int bits, group_eff, scale_dtype;
+  int n, k;
+  const void* bias;
+  void* logits;
+  int topk;
+  int32_t* topk_idx;
+  float* topk_val;
+  unsigned int* counter;      // zero between calls; the last CTA resets it
+  unsigned long long* cand;   // [m][WQL_MAX_CTAS][topk] keys
+  float* scratch;             // [m][n] fp32 logits (top-K input)
+};
+// Bandwidth-bound path for m <= 16 (warp-level MMA, split over vocab rows).
+cudaError_t launch_decode(const LogitsArgs& a, cudaStream_t s);
+
+struct RescoreArgs {
+  const void* x;
+  int x_dtype;
+  int m, n, k;
+  const void* w_ref;
+  const void* bias;
+  int topk;
+  int32_t* topk_idx;
+  float* topk_val;
+  void* logits;
+};
+cudaError_t launch_rescore(const RescoreArgs& a, cudaStream_t s);
+
+// Workspace layout shared by the launchers and wql_workspace_size().
+struct WorkspaceLayout {
+  size_t counter_off, cand_off, scratch_off, total;
+};
+WorkspaceLayout workspace_layout(int64_t m, int64_t n, int32_t topk);
+
+}  // namespace wql
