@@ -65,10 +65,13 @@ typedef enum wql_clip {
 } wql_clip;
 
 /* A quantised lm_head weight as produced by wql_quantize().
- *   bits 4: qweight is int32 [n, k/8]; element k = 8i + j of a row is the
- *           nibble in bits [4j, 4j + 4) of word i (least significant first);
- *           nibble = q + 8.  (The page's in-word "ExLlama shuffle" order is
- *           not defined there; this natural order is this library's format.)
+ *   bits 4: qweight is int32 [n, k/8]; word i of a row holds elements
+ *           8i .. 8i+7, element 8i + j in the nibble at position
+ *           p = 4*(j % 2) + j/2 (bits [4p, 4p + 4)): even elements fill bits
+ *           0..15, odd elements bits 16..31, each ascending; nibble = q + 8.
+ *           (The pages pack in an "ExLlama shuffle" order they do not define;
+ *           this interleave is this library's format, chosen so that one
+ *           mask per 16-bit half yields an adjacent element pair.)
  *   bits 8: qweight is int8 [n, k], two's complement q in [-127, 127].
  *   scales: [n, k / group] of scale_dtype, or [n, 1] when group == 0.
  * Requirements: k % 64 == 0; group is 0 or a multiple of 64 dividing k;
@@ -107,7 +110,8 @@ wql_status wql_quantize(const void* w, int32_t w_dtype, int64_t n, int64_t k,
                         cudaStream_t stream);
 
 /* Pack nibbles (uint8 [n, k], values 0..15; higher bits are ignored) into the
- * int4 layout of wql_weight: packed_out int32 [n, k/8].  k % 8 == 0. */
+ * int4 layout of wql_weight: packed_out int32 [n, k/8].  k % 8 == 0;
+ * nibbles 8-byte aligned. */
 wql_status wql_pack(const uint8_t* nibbles, int64_t n, int64_t k,
                     int32_t* packed_out, cudaStream_t stream);
 

@@ -14,8 +14,9 @@ it with numpy arrays.  Each wrapper names the page section it follows:
   rounded before q is chosen); int8 per "Fused WNA16 GEMM for tied quantized
   lm_head logits", Perf-evals rows W8-g128 and reviewer comment item 1.
 * ``pack_int4`` / ``unpack_int4`` -- same page, Purpose ("packed along the
-  input/hidden dim"), [N, K/8] int32 words; nibble order is this library's
-  natural order (element 8i+j in bits 4j..4j+3 of word i).
+  input/hidden dim"), [N, K/8] int32 words; the in-word order is this
+  library's: element 8i+j in nibble 4*(j%2) + j//2 of word i (even elements
+  in bits 0..15, odd elements in bits 16..31).
 * ``logits``     -- same page, Purpose: logits = X . dequant(Wq)^T, the dense
   weight never needed; binary64, k ascending.
 * ``topk`` / ``rescore`` -- same page, reviewer comment item 2.

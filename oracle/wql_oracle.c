@@ -15,7 +15,10 @@
  *    ratio replaces the kept one only when its squared error is strictly
  *    smaller.
  *  - "Fused WNA16 GEMM for tied quantized lm_head logits", Purpose: the
- *    weight is packed along the hidden (input) dimension; the logits are
+ *    weight is packed along the hidden (input) dimension, eight codes per
+ *    32-bit word (radiance_lmhead_int4.py: [N, K/8] int32); the in-word order
+ *    the pages use is not defined there, so this library defines its own
+ *    (see Packing below); the logits are
  *    X . dequant(Wq)^T.  Perf-evals table rows "W8-g128" and the reviewer
  *    comment (item 1) for int8 weights with per-group or per-row scales.
  *  - same page, reviewer comment item 2: take the top-K of the quantised
@@ -262,8 +265,13 @@ int oracle_quantize(const void* w, int w_dtype, int64_t n, int64_t k, int bits,
 }
 
 /* ------------------------------------------------------------------------ */
-/* Packing: element k = 8i + j of a row sits in bits [4j, 4j+4) of word i.   */
+/* Packing: word i of a row holds elements 8i .. 8i+7; element 8i + j sits   */
+/* in nibble position p(j) = 4*(j % 2) + j / 2, i.e. bits [4p, 4p+4): the    */
+/* even elements fill bits 0..15 and the odd elements bits 16..31, each in   */
+/* ascending order.                                                          */
 /* ------------------------------------------------------------------------ */
+
+static int nibble_pos(int j) { return 4 * (j % 2) + j / 2; }
 
 int oracle_pack_int4(const uint8_t* nib, int64_t n, int64_t k, uint32_t* packed) {
   if (k % 8 != 0) return -1;
@@ -271,7 +279,7 @@ int oracle_pack_int4(const uint8_t* nib, int64_t n, int64_t k, uint32_t* packed)
     for (int64_t i = 0; i < k / 8; ++i) {
       uint32_t word = 0;
       for (int j = 0; j < 8; ++j)
-        word |= ((uint32_t)(nib[r * k + 8 * i + j] & 15u)) << (4 * j);
+        word |= ((uint32_t)(nib[r * k + 8 * i + j] & 15u)) << (4 * nibble_pos(j));
       packed[r * (k / 8) + i] = word;
     }
   return 0;
@@ -284,7 +292,7 @@ int oracle_pack_codes_int4(const int8_t* q, int64_t n, int64_t k, uint32_t* pack
     for (int64_t i = 0; i < k / 8; ++i) {
       uint32_t word = 0;
       for (int j = 0; j < 8; ++j)
-        word |= ((uint32_t)(q[r * k + 8 * i + j] + 8) & 15u) << (4 * j);
+        word |= ((uint32_t)(q[r * k + 8 * i + j] + 8) & 15u) << (4 * nibble_pos(j));
       packed[r * (k / 8) + i] = word;
     }
   return 0;
@@ -295,7 +303,7 @@ int oracle_unpack_int4(const uint32_t* packed, int64_t n, int64_t k, uint8_t* ni
   for (int64_t r = 0; r < n; ++r)
     for (int64_t kk = 0; kk < k; ++kk) {
       uint32_t word = packed[r * (k / 8) + kk / 8];
-      nib[r * k + kk] = (uint8_t)((word >> (4 * (kk % 8))) & 15u);
+      nib[r * k + kk] = (uint8_t)((word >> (4 * nibble_pos((int)(kk % 8)))) & 15u);
     }
   return 0;
 }
@@ -321,7 +329,7 @@ static double dequant(const logits_job* J, const double* srow, int64_t row, int6
   if (J->bits == 4) {
     const uint32_t* P = (const uint32_t*)J->qweight;
     uint32_t word = P[row * (J->k / 8) + kk / 8];
-    int nibble = (int)((word >> (4 * (kk % 8))) & 15u);
+    int nibble = (int)((word >> (4 * nibble_pos((int)(kk % 8)))) & 15u);
     q = nibble - 8;
   } else {
     q = (int)((const int8_t*)J->qweight)[row * J->k + kk];

@@ -35,6 +35,9 @@ TORCH_OF = {oracle.F32: torch.float32, oracle.F16: torch.float16, oracle.BF16: t
 def _lib():
     torch.cuda.set_device(DEV)
     wql.load()
+    yield
+    # no bounded wait inside any kernel may have timed out
+    assert wql.default_workspace(DEV).error_word() == 0
 
 
 def _make(n, k, scheme, seed=0):

@@ -115,7 +115,7 @@ def test_pack_every_value_every_position(oracle_mod):
             r = [0] * 8
             r[j] = v
             rows.append(r)
-            expect.append(v << (4 * j))
+            expect.append(v << (4 * (4 * (j % 2) + j // 2)))
     words = oracle.pack_int4(np.array(rows, dtype=np.uint8)).view(np.uint32)[:, 0]
     np.testing.assert_array_equal(words, np.array(expect, dtype=np.uint32))
 

@@ -158,6 +158,13 @@ class Workspace:
             self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
         return self.buf
 
+    def error_word(self) -> int:
+        """The kernels' sticky error word (0 = no bounded wait ever timed out).
+        Reads device memory, so it synchronises with the current stream."""
+        if self.buf is None:
+            return 0
+        return int(self.buf[4:8].view(torch.int32).item())
+
 
 _default_ws: dict = {}
 
@@ -214,6 +221,11 @@ def wql_unpack(packed: torch.Tensor, k: int) -> torch.Tensor:
     return out
 
 
+def default_workspace(device=None) -> Workspace:
+    dev = torch.device(device or "cuda")
+    return _default_ws.setdefault((dev, torch.cuda.current_stream(dev)), Workspace(dev))
+
+
 def wql_logits(x: torch.Tensor, qw: QuantizedWeight, bias: torch.Tensor | None = None,
                topk: int = 0, workspace: Workspace | None = None,
                out: torch.Tensor | None = None, topk_idx: torch.Tensor | None = None,
@@ -236,8 +248,7 @@ def wql_logits(x: torch.Tensor, qw: QuantizedWeight, bias: torch.Tensor | None =
             topk_val = torch.empty((m, topk), dtype=torch.float32, device=x.device)
     need = wql_workspace_size(m, qw.n, topk)
     if workspace is None:
-        workspace = _default_ws.setdefault((x.device, torch.cuda.current_stream(x.device)),
-                                           Workspace(x.device))
+        workspace = default_workspace(x.device)
     ws = workspace.get(need)
     st = qw._struct()
     _check("wql_logits", lib.wql_logits(

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(128) quantize_kernel(const QuantizeArgs a) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int q = code_of(load_w(w, j8 + j), s, qmin, qmax);
-        word |= (uint32_t)(q + 8) << (4 * j);
+        word |= (uint32_t)(q + 8) << (4 * nibble_pos(j));
       }
       out[j8 / 8] = word;
     }
@@ -107,9 +107,10 @@ __global__ void pack_kernel(const uint8_t* nib, int64_t words, uint32_t* out) {
   const uint2 v = *reinterpret_cast<const uint2*>(nib + 8 * i);
   uint32_t word = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) word |= ((v.x >> (8 * j)) & 15u) << (4 * j);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) word |= ((v.y >> (8 * j)) & 15u) << (4 * (j + 4));
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t b = ((j < 4 ? v.x : v.y) >> (8 * (j & 3))) & 15u;
+    word |= b << (4 * nibble_pos(j));
+  }
   out[i] = word;
 }
 
@@ -117,10 +118,12 @@ __global__ void unpack_kernel(const uint32_t* packed, int64_t words, uint8_t* ou
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= words) return;
   const uint32_t w = packed[i];
-  uint2 v;
-  v.x = (w & 15u) | ((w >> 4) & 15u) << 8 | ((w >> 8) & 15u) << 16 | ((w >> 12) & 15u) << 24;
-  v.y = ((w >> 16) & 15u) | ((w >> 20) & 15u) << 8 | ((w >> 24) & 15u) << 16 |
-        ((w >> 28) & 15u) << 24;
+  uint2 v = make_uint2(0u, 0u);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t b = (w >> (4 * nibble_pos(j))) & 15u;
+    if (j < 4) v.x |= b << (8 * j); else v.y |= b << (8 * (j - 4));
+  }
   *reinterpret_cast<uint2*>(out + 8 * i) = v;
 }
 

@@ -8,15 +8,53 @@
 #include <cstring>
 #include <string>
 
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "sm100.cuh"
 #include "wql_common.cuh"
 
 namespace wql {
 
 namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void resolve_encoder() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+}  // namespace
+
+cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t cols,
+                         uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols,
+                         uint32_t box_rows, Swizzle swz) {
+  std::call_once(g_encode_once, resolve_encoder);
+  if (!g_encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const CUresult r = g_encode(
+      map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+      CU_TENSOR_MAP_INTERLEAVE_NONE,
+      swz == Swizzle::k128B ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+namespace {
 std::atomic<uint64_t> g_launches{0};
 thread_local std::string g_last_error;
 constexpr int kDecodeMaxTokens = 16;
-constexpr size_t kDecodeSmemBudget = 200 * 1024;
+constexpr size_t kDecodeSmemBudget = 227 * 1024;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool half_dtype(int d) { return d == WQL_F16 || d == WQL_BF16; }
@@ -166,11 +204,10 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   if (topk > 0 && (!workspace || ws_bytes < lay.total || !aligned(workspace, 256)))
     return WQL_EWORKSPACE;
   const int esz = 2;
-  // tokens per decode launch: the activations of one launch are staged in
-  // shared memory
-  int64_t chunk = kDecodeMaxTokens;
-  while (chunk > 1 && (size_t)chunk * (size_t)k * esz > kDecodeSmemBudget) --chunk;
-  if ((size_t)k * esz > kDecodeSmemBudget) return WQL_EUNSUPPORTED;
+  const int64_t chunk = kDecodeMaxTokens;   // tokens per decode launch
+  if (decode_smem_bytes((int)(m < chunk ? m : chunk), (int)k, w->bits, (int)g) >
+      kDecodeSmemBudget)
+    return WQL_EUNSUPPORTED;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   for (int64_t m0 = 0; m0 < m; m0 += chunk) {
@@ -196,7 +233,8 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
       a.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
       a.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
     }
-    cudaError_t e = launch_decode(a, stream);
+    cudaError_t e = launch_decode(a, reinterpret_cast<unsigned int*>(ws + lay.counter_off) + 1,
+                                  stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return WQL_OK;

@@ -17,6 +17,11 @@ namespace wql {
 void note_launch();                 // one kernel launched through the library
 int device_sm_count();              // SMs of the current device (cached)
 
+// Packed int4 layout: element 8i + j of a row is the nibble at position
+// nibble_pos(j) of word i -- even elements in bits 0..15, odd in 16..31 -- so
+// that masking one nibble per 16-bit half yields the adjacent pair (j, j+1).
+__host__ __device__ constexpr int nibble_pos(int j) { return 4 * (j % 2) + j / 2; }
+
 // ---------------------------------------------------------------------------
 // Element access
 // ---------------------------------------------------------------------------
@@ -90,15 +95,20 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 __device__ __forceinline__ uint32_t bfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 
-// One 32-bit word of eight nibbles (element j in bits 4j..4j+3) -> four
-// packed pairs of exact codes q = nibble - 8:
-//   out[j] = (q[j], q[j + 4]) for j = 0..3  (low half = first element).
+// One packed 32-bit word (element j at nibble_pos(j)) -> four packed pairs of
+// exact codes q = nibble - 8 in natural order:
+//   out[p] = (q[2p], q[2p + 1]) for p = 0..3  (low half = first element).
 template <typename XT> struct Int4Dequant;
 
 template <> struct Int4Dequant<__half> {
@@ -160,6 +170,86 @@ template <> struct Int8Dequant<__nv_bfloat16> {
 };
 
 // ---------------------------------------------------------------------------
+// Offset codes for the decode path: the same magic-number trick without the
+// packed subtract.  Each 16-bit value is exactly kMagic + u (u the unsigned
+// code), so an MMA with activations x accumulates sum x*(q + kOffset) and the
+// caller subtracts kOffset * sum(x) once per scale group.  Products are exact
+// (<= 11 x 11 significant bits); the subtraction happens in fp32.
+// kOffset == 0 marks a variant that already yields exact q.
+// ---------------------------------------------------------------------------
+template <int BITS, typename XT> struct OffsetCodes;
+
+template <> struct OffsetCodes<4, __half> {   // 1024 + u, u = q + 8
+  static constexpr float kOffset = 1032.0f;
+  static constexpr int kPairs = 4;
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t (&out)[4]) {
+    const uint32_t m = 0x64006400u;
+    out[0] = lop3_and_or(w, 0x000F000Fu, m);
+    out[1] = lop3_and_or(w >> 4, 0x000F000Fu, m);
+    out[2] = lop3_and_or(w >> 8, 0x000F000Fu, m);
+    out[3] = lop3_and_or(w >> 12, 0x000F000Fu, m);
+  }
+};
+
+template <> struct OffsetCodes<4, __nv_bfloat16> {   // 128 + u, u = q + 8
+  static constexpr float kOffset = 136.0f;
+  static constexpr int kPairs = 4;
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t (&out)[4]) {
+    const uint32_t m = 0x43004300u;
+    out[0] = lop3_and_or(w, 0x000F000Fu, m);
+    out[1] = lop3_and_or(w >> 4, 0x000F000Fu, m);
+    out[2] = lop3_and_or(w >> 8, 0x000F000Fu, m);
+    out[3] = lop3_and_or(w >> 12, 0x000F000Fu, m);
+  }
+};
+
+template <> struct OffsetCodes<8, __half> {   // 1024 + b, b = q + 128
+  static constexpr float kOffset = 1152.0f;
+  static constexpr int kPairs = 2;
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t (&out)[2]) {
+    const uint32_t b = w ^ 0x80808080u;
+    out[0] = prmt(b, 0x64646464u, 0x4140u);
+    out[1] = prmt(b, 0x64646464u, 0x4342u);
+  }
+};
+
+template <> struct OffsetCodes<8, __nv_bfloat16> {   // exact q (no offset)
+  static constexpr float kOffset = 0.0f;
+  static constexpr int kPairs = 2;
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t (&out)[2]) {
+    Int8Dequant<__nv_bfloat16>::run(w, out);
+  }
+};
+
+// fp16 int4 with activations pre-scaled by 1/16 at the elements held in
+// nibbles 1 and 3 of each half-word (elements 2, 3, 6, 7 of a word): those
+// nibbles stay where they are and read as 1024 + 16u, so only one shift per
+// word is needed.  With x' = x/16 there, x'*(1024 + 16u) = 16x'*(q + 72), so
+// the per-group offset is 1032*sum(x) over the other elements plus
+// 1152*sum(x') over these.
+struct Int4F16Scaled {
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t (&out)[4]) {
+    const uint32_t m = 0x64006400u;
+    const uint32_t hi = w >> 8;
+    out[0] = lop3_and_or(w, 0x000F000Fu, m);    // elements 0, 1: 1024 + u
+    out[1] = lop3_and_or(w, 0x00F000F0u, m);    // elements 2, 3: 1024 + 16u
+    out[2] = lop3_and_or(hi, 0x000F000Fu, m);   // elements 4, 5
+    out[3] = lop3_and_or(hi, 0x00F000F0u, m);   // elements 6, 7
+  }
+};
+
+template <typename ST>
+__device__ __forceinline__ float scale_bits_to_f32(uint16_t bits);
+template <>
+__device__ __forceinline__ float scale_bits_to_f32<__half>(uint16_t bits) {
+  return __half2float(__ushort_as_half(bits));
+}
+template <>
+__device__ __forceinline__ float scale_bits_to_f32<__nv_bfloat16>(uint16_t bits) {
+  return __uint_as_float((uint32_t)bits << 16);
+}
+
+// ---------------------------------------------------------------------------
 // Warp-level tensor-core MMA (m16n8k16, fp32 accumulate)
 // ---------------------------------------------------------------------------
 template <typename XT> struct Mma16816;
@@ -167,7 +257,7 @@ template <typename XT> struct Mma16816;
 template <> struct Mma16816<__half> {
   static __device__ __forceinline__ void run(float d[4], const uint32_t a[4], uint32_t b0,
                                              uint32_t b1, const float c[4]) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
         "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -179,7 +269,7 @@ template <> struct Mma16816<__half> {
 template <> struct Mma16816<__nv_bfloat16> {
   static __device__ __forceinline__ void run(float d[4], const uint32_t a[4], uint32_t b0,
                                              uint32_t b1, const float c[4]) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
         "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -263,6 +353,36 @@ __device__ __forceinline__ void warp_merge_topk(unsigned long long (&list)[K], i
   }
 }
 
+__device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+// Same contract as warp_merge_topk, with each round's warp maximum taken by two
+// hardware reductions (value half, then index half among the tied lanes).
+template <int K>
+__device__ __forceinline__ void warp_merge_topk_redux(unsigned long long (&list)[K], int kk,
+                                                      unsigned long long (&out)[K]) {
+#pragma unroll
+  for (int r = 0; r < K; ++r) {
+    if (r < kk) {
+      const uint32_t hi = (uint32_t)(list[0] >> 32), lo = (uint32_t)list[0];
+      const uint32_t mhi = redux_max_u32(hi);
+      const uint32_t mlo = redux_max_u32(hi == mhi ? lo : 0u);
+      const unsigned long long best = ((unsigned long long)mhi << 32) | mlo;
+      out[r] = best;
+      if (list[0] == best && best != kEmptyKey) {
+#pragma unroll
+        for (int i = 0; i < K - 1; ++i) list[i] = list[i + 1];
+        list[K - 1] = kEmptyKey;
+      }
+    } else {
+      out[r] = kEmptyKey;
+    }
+  }
+}
+
 // best[lane] without dynamic register indexing (which would go to local memory)
 template <int K>
 __device__ __forceinline__ unsigned long long pick(const unsigned long long (&v)[K], int i) {
@@ -306,8 +426,10 @@ struct LogitsArgs {
   unsigned long long* cand;   // [m][WQL_MAX_CTAS][topk] keys
   float* scratch;             // [m][n] fp32 logits (top-K input)
 };
-// Bandwidth-bound path for m <= 16 (warp-level MMA, split over vocab rows).
-cudaError_t launch_decode(const LogitsArgs& a, cudaStream_t s);
+// Bandwidth-bound path for m <= 16 (TMA-fed warp MMA, split over vocab rows).
+// `err` is the workspace's sticky error word.
+cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s);
+size_t decode_smem_bytes(int m, int k, int bits, int group_eff);
 
 struct RescoreArgs {
   const void* x;
