@@ -190,3 +190,26 @@ def test_workspace_reuse_across_calls():
         torch.cuda.synchronize()
         for r in range(3):
             check_topk(idx.cpu().numpy()[r], val.cpu().numpy()[r], ref[r], absacc[r], 8)
+
+
+TC_SCHEMES = [s for s in SCHEMES if s[4] == oracle.F16 and s[2] == oracle.F16]
+
+
+@pytest.mark.parametrize("scheme", TC_SCHEMES, ids=lambda s: f"w{s[0]}g{s[1]}")
+@pytest.mark.parametrize("m,n", [(32, 1000), (48, 4099), (100, 1000), (256, 777), (300, 600)])
+def test_logits_tensor_core_path(scheme, m, n):
+    """m > 16 with fp16 activations runs the tcgen05 kernel (up to 256 tokens
+    per launch, several launches beyond)."""
+    k, K = 512, 8
+    bits, group, sdt, wdt, xdt, clip = scheme
+    w, qw, o_qw, o_s = _make(n, k, scheme, seed=m + n)
+    x = synth.activations(m, k, xdt, seed=200 + m)
+    b = synth.bias(n, xdt)
+    logits, idx, val = wql.wql_logits(x.to(DEV), qw, bias=b.to(DEV), topk=K)
+    torch.cuda.synchronize()
+    ref, absacc = oracle.logits(np_input(x, xdt), xdt, o_qw, bits, o_s, sdt, group, n, k,
+                                bias=np_bits(b), nthreads=8)
+    assert_logits_close(to_f64(logits), ref, absacc, f"m={m} n={n}")
+    g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
+    ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K) for r in range(m))
+    assert ties <= max(1, m // 8)

@@ -1,0 +1,735 @@
+// tc_gemm.cu -- logits of a weight-only quantised lm_head for larger token
+// counts (m > 16) on the 5th-generation tensor cores ("Fused WNA16 GEMM for
+// tied quantized lm_head logits", Perf evals rows M = 32 and M = 256, where
+// the product becomes a dense contraction).
+//
+// Design (sm_103a, one persistent CTA per SM, fp16 activations):
+//  * Swap AB: a 128-row vocab tile is the MMA M dimension, the tokens
+//    (padded to a multiple of 16, at most 256) are N; the fp32 accumulator
+//    lives in tensor memory, double-buffered (2N <= 512 columns) so one
+//    tile's epilogue overlaps the next tile's MMAs.
+//  * Warp 0 (one lane) streams, by TMA, the packed weight in chunks of 128
+//    bytes per row (256 int4 / 128 int8 codes; 128-row 128B-swizzled boxes)
+//    and -- unless they stay resident for the whole launch -- the
+//    activations in 64-column boxes.
+//  * Warps 2..9 dequantise: thread pair (r, r+128) owns row r of the tile;
+//    per 64-column block each turns 32 codes into exact fp16 q (magic-number
+//    LOP3/PRMT), multiplies by the row's group scale (one fp16 rounding of
+//    q*s) and writes its half of the 128B-swizzled K-major A row the tensor
+//    core reads.
+//  * Warp 1 allocates tensor memory and one lane issues tcgen05.mma
+//    (kind::f16, 128 x N x 16) for every 16 columns, committing to
+//    mbarriers that release the A / activation buffers and hand finished
+//    accumulators to the epilogue.
+//  * Warps 10..13 (one per TMEM lane quarter) read the accumulator with
+//    tcgen05.ld, add the bias, round to fp16 and store the logits.  For top-K
+//    they pass each 32-token slab through shared memory so that every warp
+//    sees all 128 rows of 8 tokens; a token whose slab holds a value at or
+//    above its running K-th best is merged into that token's list (kept in
+//    shared memory for the CTA's whole row range, owned by one warp).  After
+//    the last tile the lists become this CTA's candidates; a small kernel
+//    (one CTA per token) merges all CTAs' candidates.
+//  * Every mbarrier wait is bounded; on a timeout the CTA records an error
+//    in the workspace, skips the remaining work and still frees its TMEM.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "sm100.cuh"
+#include "wql_common.cuh"
+
+namespace wql {
+namespace {
+
+constexpr int kTileRows = 128;
+constexpr int kWarps = 14;
+constexpr int kThreads = kWarps * 32;
+constexpr int kProducerWarp = 0, kMmaWarp = 1, kDequantWarp0 = 2, kEpilogueWarp0 = 10;
+constexpr int kDequantWarps = 8, kEpilogueWarps = 4;
+constexpr int kWChunkBytes = kTileRows * 128;     // one packed-weight chunk (16 KB)
+constexpr int kABytes = kTileRows * 128;          // one 64-column fp16 A block (16 KB)
+constexpr int kWStages = 3, kAStages = 3;
+constexpr int kSlabPitch = 33;                    // floats per slab row (bank spread)
+constexpr int kSlabBytes = (kTileRows * kSlabPitch + 32) * 4;   // 128 rows x 32 tokens, fp32
+constexpr uint32_t kEpilogueBarrier = 3;          // named barrier of the epilogue warps
+
+struct TcParams {
+  LogitsArgs a;
+  int tiles_total;      // ceil(n / 128)
+  int npad;             // tokens padded to a multiple of 16
+  int kblocks;          // k / 64
+  int chunks;           // packed chunks per row
+  int ngroups;
+  int x_resident;       // activations staged once per CTA
+  int xstages;          // activation ring depth when not resident
+  int acc_bufs;         // 1 or 2 accumulators in TMEM
+  uint32_t tmem_cols;   // power of two >= acc_bufs * npad
+  uint32_t off_w, off_a, off_x, off_bar, off_slab, off_list, off_s;
+  int sbuf_bytes;       // one tile's scale rows (128 x ngroups halves), 0 = no staging
+  int scales_aligned;   // scale table 16-byte aligned
+  unsigned int* err;
+};
+
+__host__ __device__ constexpr uint32_t rup(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// ---- tcgen05 / UMMA helpers (inline PTX) ----
+// Shared-memory matrix descriptor for a K-major, 128B-swizzled operand whose
+// 8-row x 128-byte atoms are stacked 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
+  d |= (uint64_t)1u << 16;                          // leading byte offset (unused here)
+  d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: 8 rows
+  d |= (uint64_t)1u << 46;                          // descriptor version for sm_100
+  d |= (uint64_t)2u << 61;                          // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16, fp16 A/B, fp32 D, both K-major, M = 128.
+__host__ __device__ constexpr uint32_t idesc_f16(int n) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(kTileRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void epilogue_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kEpilogueBarrier), "n"(kEpilogueWarps * 32) : "memory");
+}
+
+// Exact fp16 codes q (pairs in natural order) times the fp16 scale pair s2.
+__device__ __forceinline__ void int4_q_times_s(uint32_t w, uint32_t s2, uint32_t (&out)[4]) {
+  uint32_t q[4];
+  Int4Dequant<__half>::run(w, q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out[i] = hmul2_u32(q[i], s2);
+}
+__device__ __forceinline__ void int8_q_times_s(uint32_t w, uint32_t s2, uint32_t (&out)[2]) {
+  uint32_t q[2];
+  Int8Dequant<__half>::run(w, q);
+  out[0] = hmul2_u32(q[0], s2);
+  out[1] = hmul2_u32(q[1], s2);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// slab element of (row, token): rows 32q..32q+31 are shifted by 8q columns so
+// that both the row-wise writes and the quad-wise reads hit distinct banks.
+__device__ __forceinline__ int slab_index(int row, int tok) {
+  return row * kSlabPitch + tok + 8 * (row >> 5);
+}
+
+// One slab (32 tokens x 128 rows of this tile) against the CTA's running
+// per-token top-K lists.  Warp w owns tokens 8w..8w+7 of the slab, one lane
+// quad per token, lane q of the quad scanning rows 32q..32q+31.  Values below
+// the token's current K-th best cannot enter and are skipped; the quad's
+// leader starts from the token's list, so K rounds of a quad-wide maximum
+// (two shuffles) yield the new list directly.
+template <int KT>
+__device__ __forceinline__ void slab_topk(const float* slab, unsigned long long* lists,
+                                          float* thr, int c0, int t, int m, int n, int K) {
+  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) & 3;
+  const int q = lane & 3;
+  const int jl = 8 * w + (lane >> 2);                 // token within the slab
+  const int tok = c0 + jl;
+  const bool live = tok < m;
+  unsigned long long list[KT];
+#pragma unroll
+  for (int i = 0; i < KT; ++i) list[i] = kEmptyKey;
+  int added = 0;
+  if (live) {
+    unsigned long long* tl = lists + (size_t)tok * WQL_MAX_TOPK;
+    if (q == 0) {
+#pragma unroll
+      for (int i = 0; i < KT; ++i) list[i] = i < K ? tl[i] : kEmptyKey;   // already sorted
+    }
+    const float t0 = thr[tok];
+    // all 32 loads first (independent), then the candidate mask, then inserts
+    float v[32];
+    const float* col = slab + slab_index(32 * q, jl);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = col[i * kSlabPitch];
+    const int row0 = t * kTileRows + 32 * q;
+    const int valid = min(32, n - row0);
+    uint32_t mask = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) mask |= (i < valid && v[i] >= t0) ? (1u << i) : 0u;
+    added = __popc(mask);
+    while (mask) {
+      const int i = __ffs(mask) - 1;
+      mask &= mask - 1;
+      float vi = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) vi = (j == i) ? v[j] : vi;
+      list_insert<KT>(list, topk_key(vi, (uint32_t)(row0 + i)));
+    }
+  }
+  if (!__any_sync(0xFFFFFFFFu, added > 0)) return;
+  unsigned long long out[KT];
+#pragma unroll
+  for (int r = 0; r < KT; ++r) {
+    if (r < K) {
+      unsigned long long best = list[0];
+      unsigned long long o = shfl_xor_u64(best, 1);
+      best = o > best ? o : best;
+      o = shfl_xor_u64(best, 2);
+      best = o > best ? o : best;
+      out[r] = best;
+      if (list[0] == best && best != kEmptyKey) {
+#pragma unroll
+        for (int i = 0; i < KT - 1; ++i) list[i] = list[i + 1];
+        list[KT - 1] = kEmptyKey;
+      }
+    } else {
+      out[r] = kEmptyKey;
+    }
+  }
+  // quads whose lanes added nothing reproduce their list unchanged
+  const bool quad_added = (__shfl_xor_sync(0xFFFFFFFFu, added, 1) + added +
+                           __shfl_xor_sync(0xFFFFFFFFu, added, 2) +
+                           __shfl_xor_sync(0xFFFFFFFFu, __shfl_xor_sync(0xFFFFFFFFu, added, 1), 2)) > 0;
+  if (live && q == 0 && quad_added) {
+    unsigned long long* tl = lists + (size_t)tok * WQL_MAX_TOPK;
+#pragma unroll
+    for (int i = 0; i < KT; ++i)
+      if (i < K) tl[i] = out[i];
+    const unsigned long long kth = pick(out, K - 1);
+    thr[tok] = kth == kEmptyKey ? -INFINITY : key_value(kth);
+  }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_logits_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
+                     const TcParams p) {
+  constexpr int kBlocksPerChunk = BITS == 4 ? 4 : 2;   // 64-column blocks per packed chunk
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.off_bar);
+  uint64_t* w_full = bars;
+  uint64_t* w_empty = w_full + kWStages;
+  uint64_t* a_full = w_empty + kWStages;
+  uint64_t* a_empty = a_full + kAStages;
+  uint64_t* x_full = a_empty + kAStages;
+  uint64_t* x_empty = x_full + 4;
+  uint64_t* acc_full = x_empty + 4;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* s_full = acc_empty + 2;        // per-tile scale rows (2 slots)
+  uint64_t* s_empty = s_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_empty + 2);
+  unsigned int* flags = tmem_slot + 1;   // [0] bad
+  float* slab = reinterpret_cast<float*>(sm + p.off_slab);                 // [32][128]
+  unsigned long long* lists = reinterpret_cast<unsigned long long*>(sm + p.off_list);
+  float* thr = reinterpret_cast<float*>(lists + (size_t)p.npad * WQL_MAX_TOPK);
+
+  const LogitsArgs& a = p.a;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = a.n, m = a.m;
+  const int T0 = (int)(((long long)p.tiles_total * blockIdx.x) / gridDim.x);
+  const int T1 = (int)(((long long)p.tiles_total * (blockIdx.x + 1)) / gridDim.x);
+  const int ntiles = T1 - T0;
+  const uint32_t xblock_bytes = (uint32_t)p.npad * 128u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(&w_full[s], 1);
+      mbar_init(&w_empty[s], kDequantWarps);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&a_full[s], kDequantWarps);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&x_full[s], 1);
+      mbar_init(&x_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], kEpilogueWarps);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], kDequantWarps);
+    }
+    flags[0] = 0u;
+    fence_barrier_init();
+  }
+  if (a.topk > 0) {
+    for (int i = threadIdx.x; i < p.npad * WQL_MAX_TOPK; i += kThreads) lists[i] = kEmptyKey;
+    for (int i = threadIdx.x; i < p.npad; i += kThreads) thr[i] = -INFINITY;
+  }
+  if (warp == kMmaWarp) {
+    // tensor-memory accumulators (one warp allocates; freed by the same warp)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(p.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  bool bad = false;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      prefetch_tmap(&tw);
+      prefetch_tmap(&tx);
+      uint8_t* xres = sm + p.off_x;
+      if (p.x_resident && ntiles > 0) {
+        // all activation blocks once, on x_full[0]; a box always moves npad
+        // rows (rows >= m are zero-filled and counted)
+        mbar_arrive_expect_tx(&x_full[0], (uint32_t)p.kblocks * xblock_bytes);
+        for (int kb = 0; kb < p.kblocks; ++kb)
+          tma_load_2d(xres + kb * xblock_bytes, &tx, kb * 64, 0, &x_full[0]);
+      }
+      int ws = 0, xs = 0;
+      uint32_t wph = 0, xph = 0;
+      int wfills = 0, xfills = 0, sfills = 0;
+      const uint8_t* scales = reinterpret_cast<const uint8_t*>(a.scales);
+      for (int t = T0; t < T1 && !bad; ++t) {
+        // this tile's scale rows, when the tile is whole and the table aligned
+        if (p.sbuf_bytes > 0 && p.scales_aligned && (t + 1) * kTileRows <= n) {
+          const int slot = sfills & 1;
+          if (sfills >= 2) bad = !mbar_wait(&s_empty[slot], (uint32_t)(((sfills - 2) >> 1) & 1));
+          if (bad) break;
+          const uint32_t sbytes = (uint32_t)(kTileRows * p.ngroups * 2);
+          mbar_arrive_expect_tx(&s_full[slot], sbytes);
+          bulk_load(sm + p.off_s + slot * p.sbuf_bytes,
+                    scales + (size_t)t * kTileRows * p.ngroups * 2, sbytes, &s_full[slot]);
+          ++sfills;
+        }
+        for (int c = 0; c < p.chunks && !bad; ++c) {
+          if (wfills >= kWStages) bad = !mbar_wait(&w_empty[ws], wph ^ 1u);
+          if (bad) break;
+          mbar_arrive_expect_tx(&w_full[ws], (uint32_t)kWChunkBytes);
+          tma_load_2d(sm + p.off_w + ws * kWChunkBytes, &tw, c * 32, t * kTileRows, &w_full[ws]);
+          ++wfills;
+          if (++ws == kWStages) { ws = 0; wph ^= 1u; }
+          if (!p.x_resident) {
+            for (int b = 0; b < kBlocksPerChunk; ++b) {
+              const int kb = c * kBlocksPerChunk + b;
+              if (kb >= p.kblocks) break;
+              if (xfills >= p.xstages) bad = !mbar_wait(&x_empty[xs], xph ^ 1u);
+              if (bad) break;
+              mbar_arrive_expect_tx(&x_full[xs], xblock_bytes);
+              tma_load_2d(sm + p.off_x + xs * xblock_bytes, &tx, kb * 64, 0, &x_full[xs]);
+              ++xfills;
+              if (++xs == p.xstages) { xs = 0; xph ^= 1u; }
+            }
+          }
+        }
+      }
+      // every issued copy lands before the CTA can finish
+      for (int s = 0; s < 2 && s < sfills; ++s)
+        if (!mbar_wait(&s_full[s], (uint32_t)(((sfills - 1 - s) >> 1) & 1))) bad = true;
+      for (int s = 0; s < kWStages && s < wfills; ++s)
+        if (!mbar_wait(&w_full[s], (uint32_t)(((wfills - 1 - s) / kWStages) & 1))) bad = true;
+      if (p.x_resident) {
+        if (ntiles > 0 && !mbar_wait(&x_full[0], 0u)) bad = true;
+      } else {
+        for (int s = 0; s < p.xstages && s < xfills; ++s)
+          if (!mbar_wait(&x_full[s], (uint32_t)(((xfills - 1 - s) / p.xstages) & 1))) bad = true;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(p.npad);
+      int as = 0, xs = 0, acc = 0;
+      uint32_t aph = 0, xph = 0, accph = 0;
+      int tiles_done = 0;
+      bool x_ready = false;
+      for (int t = T0; t < T1 && !bad; ++t, ++tiles_done) {
+        // wait for the epilogue to have drained this accumulator buffer
+        if (tiles_done >= p.acc_bufs) bad = !mbar_wait(&acc_empty[acc], accph ^ 1u);
+        if (bad) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.npad);
+        for (int kb = 0; kb < p.kblocks && !bad; ++kb) {
+          bad = !mbar_wait(&a_full[as], aph);
+          if (!bad) {
+            if (p.x_resident) {
+              if (!x_ready) {
+                bad = !mbar_wait(&x_full[0], 0u);
+                x_ready = true;
+              }
+            } else {
+              bad = !mbar_wait(&x_full[xs], xph);
+            }
+          }
+          if (bad) break;
+          tc_fence_after();
+          const uint32_t a_addr = base + p.off_a + as * kABytes;
+          const uint32_t x_addr = p.x_resident ? base + p.off_x + kb * xblock_bytes
+                                               : base + p.off_x + xs * xblock_bytes;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_f16(d_tmem, smem_desc_sw128(a_addr + ks * 32), smem_desc_sw128(x_addr + ks * 32),
+                     idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&a_empty[as]);            // A block consumed
+          if (++as == kAStages) { as = 0; aph ^= 1u; }
+          if (!p.x_resident) {
+            umma_commit(&x_empty[xs]);          // activation block consumed
+            if (++xs == p.xstages) { xs = 0; xph ^= 1u; }
+          }
+        }
+        if (bad) break;
+        umma_commit(&acc_full[acc]);            // accumulator ready for the epilogue
+        if (++acc == p.acc_bufs) { acc = 0; accph ^= 1u; }
+      }
+    }
+  } else if (warp < kEpilogueWarp0) {
+    // ------------------------------ dequantisers ------------------------------
+    const int tdq = threadIdx.x - kDequantWarp0 * 32;     // 0..255
+    const int r = tdq & (kTileRows - 1);                   // row of the tile
+    const int half = tdq >> 7;                             // which 32 codes of a block
+    const uint32_t sw = (uint32_t)(r & 7);
+    int ws = 0, as = 0;
+    uint32_t wph = 0, aph = 0;
+    int afills = 0, sfills = 0;
+    const int gblocks = a.group_eff / 64;                  // 64-column blocks per group
+    for (int t = T0; t < T1; ++t) {
+      const int row = min(t * kTileRows + r, n - 1);
+      const bool staged = p.sbuf_bytes > 0 && p.scales_aligned && (t + 1) * kTileRows <= n;
+      const int slot = sfills & 1;
+      const uint16_t* srow;
+      if (staged) {
+        if (!bad) bad = !mbar_wait(&s_full[slot], (uint32_t)((sfills >> 1) & 1));
+        srow = reinterpret_cast<const uint16_t*>(sm + p.off_s + slot * p.sbuf_bytes) +
+               r * p.ngroups;
+      } else {
+        srow = a.scales + (size_t)row * p.ngroups;
+      }
+      int kb = 0, gi = 0, bin = 0;
+      for (int c = 0; c < p.chunks; ++c) {
+        if (!bad) bad = !mbar_wait(&w_full[ws], wph);
+        const uint32_t wrow = base + p.off_w + ws * kWChunkBytes + r * 128;
+        for (int b = 0; b < kBlocksPerChunk && kb < p.kblocks; ++b, ++kb) {
+          if (afills >= kAStages && !bad) bad = !mbar_wait(&a_empty[as], aph ^ 1u);
+          if (!bad) {
+            const uint16_t sbits = staged ? srow[gi] : ldg_u16(srow + gi);
+            const uint32_t s2 = (uint32_t)sbits | ((uint32_t)sbits << 16);
+            const uint32_t arow = base + p.off_a + as * kABytes + r * 128;
+            if constexpr (BITS == 4) {
+              // 16 packed bytes = 32 codes = A chunks 4*half .. 4*half+3
+              const uint32_t piece = (uint32_t)(2 * b + half) ^ sw;
+              const uint4 v = lds128(wrow + piece * 16);
+              const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int wdi = 0; wdi < 4; ++wdi) {
+                uint32_t o[4];
+                int4_q_times_s(words[wdi], s2, o);
+                const uint32_t chunk = (uint32_t)(4 * half + wdi) ^ sw;
+                st_shared_v4(arow + chunk * 16, o[0], o[1], o[2], o[3]);
+              }
+            } else {
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const int h = 2 * half + h2;                // 16 codes per packed piece
+                const uint32_t piece = (uint32_t)(4 * b + h) ^ sw;
+                const uint4 v = lds128(wrow + piece * 16);
+                uint32_t o0[2], o1[2], o2[2], o3[2];
+                int8_q_times_s(v.x, s2, o0);
+                int8_q_times_s(v.y, s2, o1);
+                int8_q_times_s(v.z, s2, o2);
+                int8_q_times_s(v.w, s2, o3);
+                st_shared_v4(arow + (((uint32_t)(2 * h) ^ sw) * 16), o0[0], o0[1], o1[0], o1[1]);
+                st_shared_v4(arow + (((uint32_t)(2 * h + 1) ^ sw) * 16), o2[0], o2[1], o3[0],
+                             o3[1]);
+              }
+            }
+            fence_async_smem();                 // generic-proxy writes -> tensor core
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[as]);
+          ++afills;
+          if (++as == kAStages) { as = 0; aph ^= 1u; }
+          if (++bin == gblocks) { bin = 0; ++gi; }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&w_empty[ws]);
+        if (++ws == kWStages) { ws = 0; wph ^= 1u; }
+      }
+      if (staged) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[slot]);
+        ++sfills;
+      }
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;
+    const int K = a.topk;
+    int acc = 0;
+    uint32_t accph = 0;
+    for (int t = T0; t < T1; ++t) {
+      if (!bad) bad = !mbar_wait(&acc_full[acc], accph);
+      tc_fence_after();
+      const int row = t * kTileRows + r;
+      const float bias = (a.bias && row < n)
+                             ? __half2float(reinterpret_cast<const __half*>(a.bias)[row])
+                             : 0.f;
+      const uint32_t taddr =
+          tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * p.npad);
+      for (int c0 = 0; c0 < p.npad; c0 += 32) {
+        uint32_t v[32];
+        if (!bad) tmem_ld32(taddr + (uint32_t)c0, v);
+        if (!bad && row < n) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int tok = c0 + j;
+            if (tok < m)
+              reinterpret_cast<__half*>(a.logits)[(size_t)tok * n + row] =
+                  __float2half_rn(__uint_as_float(v[j]) + bias);
+          }
+        }
+        if (K > 0) {
+          // this warp's 32 rows of the slab's 32 tokens
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            slab[slab_index(r, j)] = __uint_as_float(v[j]) + bias;
+          epilogue_sync();
+          if (!bad) {
+            if (K <= 8)
+              slab_topk<8>(slab, lists, thr, c0, t, m, n, K);
+            else
+              slab_topk<16>(slab, lists, thr, c0, t, m, n, K);
+          }
+          epilogue_sync();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (++acc == p.acc_bufs) { acc = 0; accph ^= 1u; }
+    }
+    // this CTA's candidates: each epilogue warp writes the lists of its tokens
+    if (K > 0 && !bad) {
+      for (int c0 = 0; c0 < m; c0 += 32)
+        for (int jj = 0; jj < 8; ++jj) {
+          const int tok = c0 + 8 * quarter + jj;
+          if (tok < m && lane < K)
+            a.cand[((size_t)tok * WQL_MAX_CTAS + blockIdx.x) * K + lane] =
+                lists[(size_t)tok * WQL_MAX_TOPK + lane];
+        }
+    }
+  }
+
+  if (bad) atomicOr(&flags[0], 1u);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(p.tmem_cols)
+                 : "memory");
+  }
+  if (flags[0] != 0u && threadIdx.x == 0) atomicOr(p.err, 2u);
+}
+
+// Final top-K of one token from every CTA's candidates (one CTA per token).
+template <int KT>
+__global__ void __launch_bounds__(256) topk_merge_kernel(const LogitsArgs a, int nctas,
+                                                         const unsigned int* err) {
+  __shared__ unsigned long long red[8 * KT];
+  const int tok = blockIdx.x, K = a.topk;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool any_bad = __ldcg(err) != 0u;
+  const unsigned long long* src = a.cand + (size_t)tok * WQL_MAX_CTAS * K;
+  unsigned long long list[KT];
+#pragma unroll
+  for (int i = 0; i < KT; ++i) list[i] = kEmptyKey;
+  const int count = any_bad ? 0 : nctas * K;
+  for (int i0 = threadIdx.x; i0 < count; i0 += 8 * 256) {
+    unsigned long long v[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+      v[b] = i0 + b * 256 < count ? __ldcg(src + i0 + b * 256) : kEmptyKey;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) list_insert<KT>(list, v[b]);
+  }
+  unsigned long long best[KT];
+  warp_merge_topk_redux<KT>(list, K, best);
+  if (lane < KT) red[warp * KT + lane] = pick(best, lane);
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long l2[KT];
+#pragma unroll
+    for (int i = 0; i < KT; ++i) l2[i] = lane < 8 ? red[lane * KT + i] : kEmptyKey;
+    warp_merge_topk_redux<KT>(l2, K, best);
+    const unsigned long long mine = pick(best, lane);
+    if (lane < K) {
+      const bool ok = !any_bad && mine != kEmptyKey;
+      a.topk_idx[(size_t)tok * K + lane] = ok ? key_index(mine) : -1;
+      a.topk_val[(size_t)tok * K + lane] = ok ? key_value(mine) : __int_as_float(0x7FC00000);
+    }
+  }
+}
+
+struct TcLayout {
+  uint32_t off_w, off_a, off_x, off_bar, off_slab, off_list, off_s;
+  size_t smem;
+  int x_resident, xstages, sbuf_bytes;
+};
+
+TcLayout tc_plan(int npad, int k, int ngroups) {
+  TcLayout L{};
+  const uint32_t xblock = (uint32_t)npad * 128u;
+  const int kblocks = k / 64;
+  const uint32_t lists = (uint32_t)npad * (WQL_MAX_TOPK * 8 + 4);
+  const uint32_t sbuf = rup((uint32_t)(kTileRows * ngroups * 2), 128u);
+  L.sbuf_bytes = (2 * sbuf <= 24u * 1024u) ? (int)sbuf : 0;   // else direct scale loads
+  const uint32_t tail = 512 + 128 + kSlabBytes + 64 + lists + 2 * L.sbuf_bytes + 128 + 1024;
+  const uint32_t limit = 227u * 1024u;
+  uint32_t off = 0;
+  L.off_w = off;
+  off += kWStages * kWChunkBytes;
+  L.off_a = off;
+  off += kAStages * kABytes;
+  L.off_x = off;
+  const uint32_t resident = (uint32_t)kblocks * xblock;
+  if (off + resident + tail <= limit) {
+    L.x_resident = 1;
+    L.xstages = 1;
+    off += resident;
+  } else {
+    L.x_resident = 0;
+    L.xstages = (off + 3 * xblock + tail <= limit) ? 3 : 2;
+    off += L.xstages * xblock;
+  }
+  L.off_bar = rup(off, 64);
+  off = L.off_bar + 512;
+  L.off_slab = rup(off, 128);
+  off = L.off_slab + kSlabBytes;
+  L.off_list = rup(off, 64);
+  off = L.off_list + lists;
+  L.off_s = rup(off, 128);
+  off = L.off_s + 2 * L.sbuf_bytes;
+  L.smem = off + 1024;
+  return L;
+}
+
+template <int BITS>
+cudaError_t tc_launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p,
+                        size_t smem, int ctas, cudaStream_t s) {
+  auto kern = tc_logits_kernel<BITS>;
+  static size_t configured = 0;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  kern<<<ctas, kThreads, smem, s>>>(tw, tx, p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(const LogitsArgs& a) {
+  if (a.x_dtype != WQL_F16 || a.scale_dtype != WQL_F16) return false;
+  if (a.m < 1 || a.m > 256 || a.k % 64 != 0) return false;
+  const int npad = (a.m + 15) / 16 * 16;
+  return tc_plan(npad, a.k, a.k / a.group_eff).smem <= 227u * 1024u;
+}
+
+cudaError_t launch_tc(const LogitsArgs& a, unsigned int* err, cudaStream_t s) {
+  if (!tc_supported(a)) return cudaErrorInvalidConfiguration;
+  TcParams p{};
+  p.a = a;
+  p.err = err;
+  p.tiles_total = (a.n + kTileRows - 1) / kTileRows;
+  p.npad = (a.m + 15) / 16 * 16;
+  p.kblocks = a.k / 64;
+  const int row_bytes = a.k * a.bits / 8;
+  p.chunks = (row_bytes + 127) / 128;
+  p.ngroups = a.k / a.group_eff;
+  p.acc_bufs = (2 * p.npad <= 512) ? 2 : 1;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(p.acc_bufs * p.npad)) cols <<= 1;
+  p.tmem_cols = cols;
+  const TcLayout L = tc_plan(p.npad, a.k, p.ngroups);
+  p.sbuf_bytes = L.sbuf_bytes;
+  p.off_s = L.off_s;
+  p.scales_aligned = (reinterpret_cast<uintptr_t>(a.scales) % 16) == 0;
+  p.x_resident = L.x_resident;
+  p.xstages = L.xstages;
+  p.off_w = L.off_w;
+  p.off_a = L.off_a;
+  p.off_x = L.off_x;
+  p.off_bar = L.off_bar;
+  p.off_slab = L.off_slab;
+  p.off_list = L.off_list;
+
+  CUtensorMap tw, tx;
+  cudaError_t e = make_tmap_2d(&tw, a.qweight, 4, (uint64_t)row_bytes / 4, (uint64_t)a.n,
+                               (uint64_t)row_bytes, 32, kTileRows, Swizzle::k128B);
+  if (e != cudaSuccess) return e;
+  // activation boxes: 64 columns x npad rows (rows >= m read as zero)
+  e = make_tmap_2d(&tx, a.x, 2, (uint64_t)a.k, (uint64_t)a.m, (uint64_t)a.k * 2, 64,
+                   (uint32_t)p.npad, Swizzle::k128B);
+  if (e != cudaSuccess) return e;
+  int ctas = device_sm_count();
+  if (ctas > p.tiles_total) ctas = p.tiles_total;
+  if (ctas > WQL_MAX_CTAS) ctas = WQL_MAX_CTAS;
+  e = a.bits == 4 ? tc_launch_t<4>(tw, tx, p, L.smem, ctas, s)
+                  : tc_launch_t<8>(tw, tx, p, L.smem, ctas, s);
+  if (e != cudaSuccess || a.topk <= 0) return e;
+  if (a.topk <= 8)
+    topk_merge_kernel<8><<<a.m, 256, 0, s>>>(a, ctas, err);
+  else
+    topk_merge_kernel<16><<<a.m, 256, 0, s>>>(a, ctas, err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace wql

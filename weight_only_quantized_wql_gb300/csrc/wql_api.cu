@@ -204,37 +204,51 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   if (topk > 0 && (!workspace || ws_bytes < lay.total || !aligned(workspace, 256)))
     return WQL_EWORKSPACE;
   const int esz = 2;
-  const int64_t chunk = kDecodeMaxTokens;   // tokens per decode launch
-  if (decode_smem_bytes((int)(m < chunk ? m : chunk), (int)k, w->bits, (int)g) >
+  const int64_t dchunk = kDecodeMaxTokens;   // tokens per decode launch
+  if (decode_smem_bytes((int)(m < dchunk ? m : dchunk), (int)k, w->bits, (int)g) >
       kDecodeSmemBudget)
     return WQL_EUNSUPPORTED;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
+  unsigned int* err_word = reinterpret_cast<unsigned int*>(ws + lay.counter_off) + 1;
+  LogitsArgs base{};
+  base.x_dtype = x_dtype;
+  base.qweight = w->qweight;
+  base.scales = static_cast<const uint16_t*>(w->scales);
+  base.bits = w->bits;
+  base.group_eff = (int)g;
+  base.scale_dtype = w->scale_dtype;
+  base.n = (int)n;
+  base.k = (int)k;
+  base.bias = bias;
+  base.topk = topk;
+  if (topk > 0) {
+    base.counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
+    base.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
+    base.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
+  }
+  // Token counts above 16 go to the tensor-core kernel (up to 256 tokens per
+  // launch) when it supports the dtype combination; otherwise the decode
+  // kernel runs on 16-token slices.
+  LogitsArgs probe = base;
+  probe.m = (int)(m < 256 ? m : 256);
+  const bool use_tc = m > kDecodeMaxTokens && tc_supported(probe);
+  const int64_t chunk = use_tc ? 256 : kDecodeMaxTokens;
   for (int64_t m0 = 0; m0 < m; m0 += chunk) {
     const int64_t mc = (m - m0) < chunk ? (m - m0) : chunk;
-    LogitsArgs a{};
+    LogitsArgs a = base;
     a.x = static_cast<const unsigned char*>(x) + (size_t)m0 * k * esz;
-    a.x_dtype = x_dtype;
     a.m = (int)mc;
-    a.qweight = w->qweight;
-    a.scales = static_cast<const uint16_t*>(w->scales);
-    a.bits = w->bits;
-    a.group_eff = (int)g;
-    a.scale_dtype = w->scale_dtype;
-    a.n = (int)n;
-    a.k = (int)k;
-    a.bias = bias;
     a.logits = static_cast<unsigned char*>(logits_out) + (size_t)m0 * n * esz;
-    a.topk = topk;
     if (topk > 0) {
       a.topk_idx = topk_idx + (size_t)m0 * topk;
       a.topk_val = topk_val + (size_t)m0 * topk;
-      a.counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
-      a.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
-      a.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
     }
-    cudaError_t e = launch_decode(a, reinterpret_cast<unsigned int*>(ws + lay.counter_off) + 1,
-                                  stream);
+    cudaError_t e;
+    if (use_tc && mc > kDecodeMaxTokens)
+      e = launch_tc(a, err_word, stream);
+    else
+      e = launch_decode(a, err_word, stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return WQL_OK;

@@ -430,6 +430,9 @@ struct LogitsArgs {
 // `err` is the workspace's sticky error word.
 cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s);
 size_t decode_smem_bytes(int m, int k, int bits, int group_eff);
+// Tensor-core path for 16 < m <= 256 (fp16 activations and scales).
+bool tc_supported(const LogitsArgs& a);
+cudaError_t launch_tc(const LogitsArgs& a, unsigned int* err, cudaStream_t s);
 
 struct RescoreArgs {
   const void* x;
