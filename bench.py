@@ -59,9 +59,9 @@ def rescore_bytes(m: int, k: int, topk: int, w_bytes: int = 2, x_bytes: int = 2)
     return m * topk * k * w_bytes + m * k * x_bytes + m * topk * (8 + 2)
 
 
-def step_bytes() -> int:
+def step_bytes(ms=MS) -> int:
     return sum(logits_bytes(m, N_VOCAB, K_HIDDEN, 4, GROUP, topk=TOPK) +
-               rescore_bytes(m, K_HIDDEN, TOPK) for m in MS)
+               rescore_bytes(m, K_HIDDEN, TOPK) for m in ms)
 
 
 # ---------------------------------------------------------------------------
@@ -162,6 +162,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     import torch
     import weight_only_quantized_wql_gb300 as wql
 
+    MS = tuple(args.ms)   # noqa: N806  (token counts timed in this run)
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     wql.load()
@@ -279,7 +280,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
         return None
 
     pk = peaks()
-    total_bytes = step_bytes() * args.steps * world
+    total_bytes = step_bytes(MS) * args.steps * world
     value = total_bytes / dev_s / 1e9
     med = {m: statistics.median(logit_us[m]) for m in MS}
     calls = {}
@@ -325,11 +326,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
                    "ms": list(MS), "topk": TOPK, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {N_COPIES} rotating weight copies "
                          f"({N_COPIES * 83} MB), each call reads a copy untouched for 3 calls",
-                   "step_bytes": step_bytes()},
+                   "step_bytes": step_bytes(MS)},
         "calls": calls, "quantize_ms": round(quant_ms, 3),
         "roofline": roof,
         "cpu_baseline": None,
-        "e2e": {"value": round(step_bytes() * args.steps * world / e2e_s / 1e9, 1),
+        "e2e": {"value": round(step_bytes(MS) * args.steps * world / e2e_s / 1e9, 1),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "wall_s_timed": round(t_wall, 4),
@@ -433,6 +434,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ms", type=int, nargs="+", default=list(MS),
+                    help="token counts M timed per step (default: 1 32 256); a subset "
+                         "is for profiling one call, not a bench line")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", "0"))
