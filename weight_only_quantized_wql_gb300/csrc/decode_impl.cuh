@@ -60,7 +60,7 @@ struct DecodeParams {
   uint32_t off_x, off_s, off_corr, off_bar, off_red;
   int sbuf_bytes, nsb;  // scale buffer size and count
   int scales_aligned;   // scale table 16-byte aligned (bulk copies allowed)
-  unsigned int* err;    // sticky error word in the workspace
+  unsigned int* err;    // sticky error word in the workspace (null: none)
 };
 
 __host__ __device__ constexpr uint32_t round_up_u32(uint32_t v, uint32_t a) {
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (bad) atomicOr(&flags[0], 1u);
   __syncthreads();
   const bool cta_bad = flags[0] != 0u;
-  if (cta_bad && threadIdx.x == 0) atomicOr(p.err, 1u);
+  if (cta_bad && threadIdx.x == 0 && p.err) atomicOr(p.err, 1u);
   if (a.topk <= 0) return;
 
   // ---------------- top-K: per-CTA selection, last-CTA merge ----------------

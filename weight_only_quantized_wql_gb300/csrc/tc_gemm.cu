@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(p.tmem_cols)
                  : "memory");
   }
-  if (flags[0] != 0u && threadIdx.x == 0) atomicOr(p.err, 2u);
+  if (flags[0] != 0u && threadIdx.x == 0 && p.err) atomicOr(p.err, 2u);
 }
 
 // Final top-K of one token from every CTA's candidates (one CTA per token).

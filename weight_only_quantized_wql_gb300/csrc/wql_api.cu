@@ -210,7 +210,9 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
     return WQL_EUNSUPPORTED;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  unsigned int* err_word = reinterpret_cast<unsigned int*>(ws + lay.counter_off) + 1;
+  // No workspace (allowed when topk == 0): the kernels skip the error word.
+  unsigned int* err_word =
+      ws ? reinterpret_cast<unsigned int*>(ws + lay.counter_off) + 1 : nullptr;
   LogitsArgs base{};
   base.x_dtype = x_dtype;
   base.qweight = w->qweight;
