@@ -22,7 +22,8 @@
  * Conventions for every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
  *     library allocates no device memory; scratch space is a caller buffer
- *     sized by wql_workspace_size().
+ *     sized by wql_workspace_size() (wql_logits_noalloc instead uses one
+ *     fixed area inside the library, see there).
  *   - Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy
  *     default stream).  Results are ready once the stream has reached them.
  *   - Arguments are checked on the host before anything is launched.  On any
@@ -143,6 +144,39 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m,
                       const wql_weight* w, const void* bias, void* logits_out,
                       int32_t topk, int32_t* topk_idx, float* topk_val,
                       void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Size of the device scratch area that wql_logits_noalloc uses: 24 MiB. */
+#define WQL_NOALLOC_SCRATCH_BYTES ((size_t)24 << 20)
+
+/* wql_logits without a workspace argument.  The pages have no counterpart:
+ * this is an interface of this library for callers that cannot provide
+ * device memory -- a host program linking only this library, with no device
+ * allocator of its own, or a serving loop that must not allocate after
+ * start-up.  Arguments, layouts and results are those of wql_logits, except:
+ *   - Scratch is one fixed area of WQL_NOALLOC_SCRATCH_BYTES per device,
+ *     inside the library (reserved by the CUDA runtime when it loads the
+ *     library's code on the device).  The call allocates nothing.
+ *   - Every token count runs the decode kernel, in slices of 16 token rows;
+ *     a call whose slice needs more scratch than the area holds, i.e.
+ *     wql_workspace_size(min(m, 16), n, topk) > WQL_NOALLOC_SCRATCH_BYTES
+ *     (with top-K: about 64 * n + 1 MiB bytes at 16 rows and topk 8), is
+ *     rejected with WQL_EWORKSPACE before anything is launched.
+ *   - The first call on each device does a one-time setup (it looks up the
+ *     area's device address with that device current); make that first call
+ *     before any stream capture begins.  A failed setup returns WQL_ECUDA and
+ *     is retried by the next call.
+ *   - The area's ticket counter and error word are cleared on `stream` at
+ *     the start of every call (one small memset before the launches).
+ *   - Calls on one device share the area: calls that may be in flight at
+ *     the same time (other streams, unsynchronised host threads) race and
+ *     corrupt each other's outputs.  Serialise them.
+ * An internal wait that timed out (a stalled GPU, never bad arguments) shows
+ * as index -1 and NaN values in topk_idx / topk_val. */
+wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t m,
+                              const wql_weight* w, const void* bias,
+                              void* logits_out, int32_t topk,
+                              int32_t* topk_idx, float* topk_val,
+                              cudaStream_t stream);
 
 /* Exact top-K rescoring ("Fused WNA16 GEMM for tied quantized lm_head
  * logits", reviewer comment item 2): for every row m and each of its topk

@@ -28,9 +28,9 @@ from . import _build
 
 __all__ = [
     "WQLError", "QuantizedWeight", "Workspace", "load", "wql_quantize", "wql_pack",
-    "wql_unpack", "wql_workspace_size", "wql_logits", "wql_topk_rescore",
+    "wql_unpack", "wql_workspace_size", "wql_logits", "wql_logits_noalloc", "wql_topk_rescore",
     "wql_status_string", "wql_last_error", "wql_launch_count", "F32", "F16", "BF16",
-    "CLIP_RTN", "CLIP_MSE", "MAX_TOPK",
+    "CLIP_RTN", "CLIP_MSE", "MAX_TOPK", "NOALLOC_SCRATCH_BYTES",
 ]
 
 F32, F16, BF16 = 0, 1, 2
@@ -47,11 +47,13 @@ _lib = None
 
 
 class WQLError(RuntimeError):
-    def __init__(self, fn: str, status: int):
+    def __init__(self, fn: str, status: int, detail: str = ""):
         self.status = status
         msg = f"{fn} failed: {_STATUS.get(status, status)}"
         if status == 3 and _lib is not None:
             msg += f" ({_lib.wql_last_error().decode()})"
+        if detail:
+            msg += f" ({detail})"
         super().__init__(msg)
 
 
@@ -90,6 +92,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wql_logits.restype = i32
         lib.wql_logits.argtypes = [vp, i32, i64, ctypes.POINTER(_WqlWeight), vp, vp, i32, vp,
                                    vp, vp, sz, vp]
+        lib.wql_logits_noalloc.restype = i32
+        lib.wql_logits_noalloc.argtypes = [vp, i32, i64, ctypes.POINTER(_WqlWeight), vp, vp,
+                                           i32, vp, vp, vp]
         lib.wql_topk_rescore.restype = i32
         lib.wql_topk_rescore.argtypes = [vp, i32, i64, vp, i32, i64, i64, vp, i32, vp, vp, vp,
                                          vp]
@@ -255,6 +260,48 @@ def wql_logits(x: torch.Tensor, qw: QuantizedWeight, bias: torch.Tensor | None =
         _ptr(x2), _DTYPE_CODE[x.dtype], m, ctypes.byref(st), _ptr(bias), _ptr(out), topk,
         _ptr(topk_idx) if topk > 0 else None, _ptr(topk_val) if topk > 0 else None,
         _ptr(ws), ws.numel(), _stream(x.device)))
+    logits = out.reshape(*lead, qw.n)
+    if topk > 0:
+        return logits, topk_idx.reshape(*lead, topk), topk_val.reshape(*lead, topk)
+    return logits, None, None
+
+
+NOALLOC_SCRATCH_BYTES = 24 << 20   # WQL_NOALLOC_SCRATCH_BYTES
+
+
+def wql_logits_noalloc(x: torch.Tensor, qw: QuantizedWeight, bias: torch.Tensor | None = None,
+                       topk: int = 0, out: torch.Tensor | None = None,
+                       topk_idx: torch.Tensor | None = None,
+                       topk_val: torch.Tensor | None = None):
+    """wql_logits through the entry point that takes no workspace: the library
+    uses its own fixed device scratch area (WQL_NOALLOC_SCRATCH_BYTES per
+    device), for callers that cannot provide device memory.  Pass `out`,
+    `topk_idx` and `topk_val` to keep this call free of allocations too (any
+    that is None is allocated here, by torch, before the library call).
+    Calls on one device share the area and must not overlap."""
+    lib = load()
+    lead = x.shape[:-1]
+    x2 = x.reshape(-1, x.shape[-1])
+    _cuda(x2, "x")
+    m = x2.shape[0]
+    if out is None:
+        out = torch.empty((m, qw.n), dtype=x.dtype, device=x.device)
+    if topk > 0:
+        if topk_idx is None:
+            topk_idx = torch.empty((m, topk), dtype=torch.int32, device=x.device)
+        if topk_val is None:
+            topk_val = torch.empty((m, topk), dtype=torch.float32, device=x.device)
+    st = qw._struct()
+    status = lib.wql_logits_noalloc(
+        _ptr(x2), _DTYPE_CODE[x.dtype], m, ctypes.byref(st), _ptr(bias), _ptr(out), topk,
+        _ptr(topk_idx) if topk > 0 else None, _ptr(topk_val) if topk > 0 else None,
+        _stream(x.device))
+    if status == 4:
+        need = wql_workspace_size(min(m, 16), qw.n, topk)
+        raise WQLError("wql_logits_noalloc", status,
+                       f"needs {need} bytes of scratch for 16-row slices of a {qw.n}-row "
+                       f"vocab with top-{topk}; the fixed area holds {NOALLOC_SCRATCH_BYTES}")
+    _check("wql_logits_noalloc", status)
     logits = out.reshape(*lead, qw.n)
     if topk > 0:
         return logits, topk_idx.reshape(*lead, topk), topk_val.reshape(*lead, topk)

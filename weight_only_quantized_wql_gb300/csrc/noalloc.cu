@@ -1,0 +1,151 @@
+// noalloc.cu -- wql_logits_noalloc: logits (+ top-K candidates) for callers
+// that cannot give the library a workspace buffer.
+//
+// Who needs it.  wql_logits wants a caller-owned device workspace for the
+// decode kernel's scratch.  Some callers have no way to make one: a host
+// program that links only this C library and has no device allocator of its
+// own, or a serving loop that reserves all of its device memory when it
+// starts and must not allocate while it runs (an allocation there can fail
+// under memory pressure, synchronise the device, or break the memory plan
+// the loop was sized with).  For them the scratch lives in one fixed-size
+// array in device memory that belongs to this library's image.  The CUDA
+// runtime reserves it when it loads this file's module on a device; this
+// entry point itself allocates nothing, and neither does anything it calls.
+//
+// What the area holds (the decode kernel's workspace, for at most 16 token
+// rows per launch): the ticket counter and the sticky error word, the per-CTA
+// top-K candidates, and the fp32 logits that the top-K selection reads back.
+// The counter and the error word must be zero when a launch starts; every
+// call clears them on its own stream before its first launch.  The rest is
+// written before it is read within each launch.
+//
+// One area per device, shared by every call on that device: calls that can
+// be in flight at the same time (on different streams, or from different
+// host threads without ordering between them) race on it and corrupt each
+// other's results.  Serialise them.
+#include <atomic>
+#include <mutex>
+
+#include "wql_common.cuh"
+
+namespace wql {
+namespace {
+
+constexpr size_t kAreaBytes = WQL_NOALLOC_SCRATCH_BYTES;
+constexpr int kSliceTokens = 16;                 // token rows per decode launch
+constexpr size_t kSmemBudget = 227 * 1024;
+constexpr int kMaxDevices = 64;
+
+// The scratch area.  Without an initialiser it is zero-filled when the
+// module is loaded and takes no room in the library file.
+static __device__ __align__(256) unsigned char g_noalloc_area[kAreaBytes];
+
+// Device address of the area, per device ordinal; null until looked up.
+std::atomic<void*> g_area_ptr[kMaxDevices];
+std::mutex g_setup_mu;
+
+// Address of the area on the current device.  The first call per device does
+// the one-time setup: with that device current, cudaGetSymbolAddress (which
+// also makes the runtime load the module there).  A failed lookup is not
+// cached, so a later call tries again.
+cudaError_t area_on_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  void* p = g_area_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    p = g_area_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+      e = cudaGetSymbolAddress(&p, g_noalloc_area);
+      if (e != cudaSuccess) return e;
+      if (p == nullptr) return cudaErrorInvalidSymbol;
+      g_area_ptr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
+bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool is_half(int d) { return d == WQL_F16 || d == WQL_BF16; }
+
+}  // namespace
+}  // namespace wql
+
+using namespace wql;
+
+extern "C" wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t m,
+                                         const wql_weight* w, const void* bias,
+                                         void* logits_out, int32_t topk, int32_t* topk_idx,
+                                         float* topk_val, cudaStream_t stream) {
+  // Host checks first: a rejected call makes no CUDA call at all.
+  if (!w || m < 0 || w->n < 0 || w->k <= 0 || w->group < 0 || w->reserved != 0)
+    return WQL_EINVAL;
+  if (topk < 0 || topk > WQL_MAX_TOPK) return WQL_EINVAL;
+  const int64_t n = w->n, k = w->k;
+  if (m > 0 && n > 0) {
+    if (!x || !w->qweight || !w->scales || !logits_out) return WQL_EINVAL;
+    if (topk > 0 && (!topk_idx || !topk_val)) return WQL_EINVAL;
+    if (topk > n) return WQL_EINVAL;
+  }
+  if (w->bits != 4 && w->bits != 8) return WQL_EUNSUPPORTED;
+  if (!is_half(x_dtype) || !is_half(w->scale_dtype)) return WQL_EUNSUPPORTED;
+  const int64_t g = w->group == 0 ? k : w->group;
+  if (k % 64 != 0 || g % 64 != 0 || k % g != 0) return WQL_EUNSUPPORTED;
+  if (n >= (int64_t(1) << 31) || m >= (int64_t(1) << 31) || k >= (int64_t(1) << 30))
+    return WQL_EUNSUPPORTED;
+  if (!is_aligned(x, 16) || !is_aligned(w->qweight, 16) || !is_aligned(w->scales, 2) ||
+      !is_aligned(logits_out, 2) || !is_aligned(bias, 2))
+    return WQL_EUNSUPPORTED;
+  if (m == 0 || n == 0) return WQL_OK;
+  const int64_t slice_max = m < kSliceTokens ? m : kSliceTokens;
+  if (decode_smem_bytes((int)slice_max, (int)k, w->bits, (int)g) > kSmemBudget)
+    return WQL_EUNSUPPORTED;
+  // Every slice reuses the same area, so one slice's layout is the need.
+  const WorkspaceLayout lay = workspace_layout(slice_max, n, topk);
+  if (lay.total > kAreaBytes) return WQL_EWORKSPACE;
+
+  void* area = nullptr;
+  cudaError_t e = area_on_current_device(&area);
+  if (e != cudaSuccess) return record_cuda_error(e);
+  unsigned char* ws = static_cast<unsigned char*>(area);
+  unsigned int* counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
+  unsigned int* err_word = counter + 1;
+  // The ticket counter and the error word start every call at zero.
+  e = cudaMemsetAsync(counter, 0, 2 * sizeof(unsigned int), stream);
+  if (e != cudaSuccess) return record_cuda_error(e);
+
+  LogitsArgs base{};
+  base.x_dtype = x_dtype;
+  base.qweight = w->qweight;
+  base.scales = static_cast<const uint16_t*>(w->scales);
+  base.bits = w->bits;
+  base.group_eff = (int)g;
+  base.scale_dtype = w->scale_dtype;
+  base.n = (int)n;
+  base.k = (int)k;
+  base.bias = bias;
+  base.topk = topk;
+  if (topk > 0) {
+    base.counter = counter;
+    base.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
+    base.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
+  }
+  const size_t esz = 2;
+  for (int64_t m0 = 0; m0 < m; m0 += kSliceTokens) {
+    const int64_t mc = (m - m0) < kSliceTokens ? (m - m0) : kSliceTokens;
+    LogitsArgs a = base;
+    a.x = static_cast<const unsigned char*>(x) + (size_t)m0 * (size_t)k * esz;
+    a.m = (int)mc;
+    a.logits = static_cast<unsigned char*>(logits_out) + (size_t)m0 * (size_t)n * esz;
+    if (topk > 0) {
+      a.topk_idx = topk_idx + (size_t)m0 * topk;
+      a.topk_val = topk_val + (size_t)m0 * topk;
+    }
+    e = launch_decode(a, err_word, stream);
+    if (e != cudaSuccess) return record_cuda_error(e);
+  }
+  return WQL_OK;
+}

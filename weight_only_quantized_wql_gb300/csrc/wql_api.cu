@@ -69,6 +69,8 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+wql_status record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 int device_sm_count() {
   static thread_local int cached_dev = -1;
   static thread_local int cached_sms = 0;

@@ -16,6 +16,7 @@ namespace wql {
 // ---------------------------------------------------------------------------
 void note_launch();                 // one kernel launched through the library
 int device_sm_count();              // SMs of the current device (cached)
+wql_status record_cuda_error(cudaError_t e);  // keep the text for wql_last_error()
 
 // Packed int4 layout: element 8i + j of a row is the nibble at position
 // nibble_pos(j) of word i -- even elements in bits 0..15, odd in 16..31 -- so
