@@ -213,3 +213,58 @@ def test_logits_tensor_core_path(scheme, m, n):
     g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
     ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K) for r in range(m))
     assert ties <= max(1, m // 8)
+
+
+@pytest.mark.parametrize("scheme", TC_SCHEMES, ids=lambda s: f"w{s[0]}g{s[1]}")
+@pytest.mark.parametrize("m", [32, 256])
+def test_tensor_core_topk_many_tiles_per_cta(scheme, m):
+    """A vocab of ~2 tiles per CTA: after each CTA's first tile the top-K runs
+    in its filtered mode (per-token thresholds, shared across CTAs)."""
+    n, k, K = 40000, 128, 8
+    bits, group, sdt, wdt, xdt, clip = scheme
+    if group and k % group:
+        pytest.skip("group does not divide k")
+    w, qw, o_qw, o_s = _make(n, k, scheme, seed=7 + m)
+    x = synth.activations(m, k, xdt, seed=300 + m)
+    logits, idx, val = wql.wql_logits(x.to(DEV), qw, topk=K)
+    torch.cuda.synchronize()
+    ref, absacc = oracle.logits(np_input(x, xdt), xdt, o_qw, bits, o_s, sdt, group, n, k,
+                                nthreads=16)
+    assert_logits_close(to_f64(logits), ref, absacc, f"m={m}")
+    g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
+    ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K) for r in range(m))
+    assert ties <= max(1, m // 8)
+
+
+def _rowwise_weight(n, k, row_value):
+    """W[r, :] = row_value(r): after quantisation every row is 7 * s_r (int4)."""
+    vals = torch.tensor([row_value(r) for r in range(n)], dtype=torch.float32)
+    return vals[:, None].expand(n, k).contiguous()
+
+
+@pytest.mark.parametrize("m", [32, 256])
+@pytest.mark.parametrize("order", ["increasing", "decreasing", "equal"])
+def test_tensor_core_topk_adversarial_orders(m, order):
+    """Logits that grow with the row index make every tile beat every
+    threshold (per-token queues overflow and the tile is redone through the
+    full selection); equal logits must give the lowest indices; decreasing
+    logits never pass after the first tile."""
+    n, k, K = 40000, 128, 8
+    f = {"increasing": lambda r: 0.01 + 1e-5 * r, "decreasing": lambda r: 0.5 - 1e-5 * r,
+         "equal": lambda r: 0.02}[order]
+    w = _rowwise_weight(n, k, f)
+    qw = wql.wql_quantize(w.to(DEV), 4, 64, torch.float16, 0)
+    o_qw, o_s = oracle_quantized(w, oracle.F32, 4, 64, oracle.F16, 0)
+    gen = torch.Generator().manual_seed(11)
+    x = (torch.rand(m, k, generator=gen) + 0.5).half()      # positive rows
+    logits, idx, val = wql.wql_logits(x.to(DEV), qw, topk=K)
+    torch.cuda.synchronize()
+    ref, absacc = oracle.logits(np_input(x, oracle.F16), oracle.F16, o_qw, 4, o_s, oracle.F16,
+                                64, n, k, nthreads=16)
+    assert_logits_close(to_f64(logits), ref, absacc, order)
+    g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
+    for r in range(m):
+        check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K)
+    if order == "equal":
+        # every row's logit is the same number: value ties go to the lowest indices
+        assert (g_idx == np.arange(K)[None, :]).all(), g_idx[:2]

@@ -90,6 +90,8 @@ WorkspaceLayout workspace_layout(int64_t m, int64_t n, int32_t topk) {
   WorkspaceLayout l{};
   l.counter_off = 0;
   size_t off = 256;
+  l.gthr_off = off;
+  if (topk > 0) off += 256 * sizeof(unsigned int);
   l.cand_off = off;
   if (topk > 0) off += round_up((size_t)m * WQL_MAX_CTAS * (size_t)topk * 8, 256);
   l.scratch_off = off;
@@ -230,6 +232,7 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
     base.counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
     base.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
     base.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
+    base.gthr = reinterpret_cast<unsigned int*>(ws + lay.gthr_off);
   }
   // Token counts above 16 go to the tensor-core kernel (up to 256 tokens per
   // launch) when it supports the dtype combination; otherwise the decode

@@ -425,7 +425,9 @@ struct LogitsArgs {
   float* topk_val;
   unsigned int* counter;      // zero between calls; the last CTA resets it
   unsigned long long* cand;   // [m][WQL_MAX_CTAS][topk] keys
-  float* scratch;             // [m][n] fp32 logits (top-K input)
+  float* scratch;             // [m][n] fp32 logits (top-K input, decode path)
+  unsigned int* gthr;         // [256] per-token K-th best seen by any CTA, orderable
+                              // bits (0 = none); zero between calls (tensor-core path)
 };
 // Bandwidth-bound path for m <= 16 (TMA-fed warp MMA, split over vocab rows).
 // `err` is the workspace's sticky error word.
@@ -450,7 +452,7 @@ cudaError_t launch_rescore(const RescoreArgs& a, cudaStream_t s);
 
 // Workspace layout shared by the launchers and wql_workspace_size().
 struct WorkspaceLayout {
-  size_t counter_off, cand_off, scratch_off, total;
+  size_t counter_off, gthr_off, cand_off, scratch_off, total;
 };
 WorkspaceLayout workspace_layout(int64_t m, int64_t n, int32_t topk);
 
