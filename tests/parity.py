@@ -64,21 +64,29 @@ def assert_logits_close(gpu: np.ndarray, ref: np.ndarray, absacc: np.ndarray, wh
 
 
 def check_topk(g_idx: np.ndarray, g_val: np.ndarray, ref_row: np.ndarray, ref_abs: np.ndarray,
-               K: int) -> int:
+               K: int, g_logits: np.ndarray | None = None) -> int:
     """Top-K candidate check for one token row against the full oracle row.
 
-    The GPU ranks fp32 logits, the oracle binary64 ones: the sets must agree
-    except for exact near-ties -- an element may be swapped only if its oracle
-    value lies within 2*delta of the oracle's K-th value, delta being the
-    largest |gpu - oracle| seen on the row's candidates.  Returns 1 if such a
-    tie swap happened, else 0.  Values must match the oracle within the logit
-    tolerance and be ordered value-descending, index-ascending."""
+    The GPU ranks its own fp32 logits, the oracle binary64 ones: the sets must
+    agree except for near-ties -- an element may be swapped only if its
+    oracle value lies within 2*delta of the oracle's K-th value, delta being
+    the largest |gpu - oracle| seen on the row's candidates (their reported
+    values and, when `g_logits` -- the row the kernel returned -- is given,
+    the returned logits at the GPU's and the oracle's candidates: candidates
+    chosen from the returned logits are exact up to their precision).
+    Returns 1 if such a tie swap happened, else 0.  Values must match the
+    oracle within the logit tolerance and be ordered value-descending,
+    index-ascending."""
     o_idx, o_val = oracle.topk(ref_row[None, :], K)
     o_idx, o_val = o_idx[0], o_val[0]
     assert np.all(g_idx >= 0) and np.all(g_idx < ref_row.shape[0])
     assert len(set(g_idx.tolist())) == K, "duplicate candidates"
     ov = ref_row[g_idx]
     delta = float(np.max(np.abs(g_val.astype(np.float64) - ov)))
+    if g_logits is not None:
+        both = np.concatenate([g_idx, o_idx])
+        delta = max(delta, float(np.max(np.abs(g_logits[both].astype(np.float64) -
+                                               ref_row[both]))))
     tol = oracle.tolerance(ref_abs[g_idx])
     assert np.all(np.abs(g_val.astype(np.float64) - ov) <= tol), "candidate values off"
     order_ok = all((g_val[i] > g_val[i + 1]) or (g_val[i] == g_val[i + 1] and g_idx[i] < g_idx[i + 1])

@@ -211,7 +211,8 @@ def test_logits_tensor_core_path(scheme, m, n):
                                 bias=np_bits(b), nthreads=8)
     assert_logits_close(to_f64(logits), ref, absacc, f"m={m} n={n}")
     g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
-    ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K) for r in range(m))
+    gl = to_f64(logits)
+    ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K, gl[r]) for r in range(m))
     assert ties <= max(1, m // 8)
 
 
@@ -232,7 +233,8 @@ def test_tensor_core_topk_many_tiles_per_cta(scheme, m):
                                 nthreads=16)
     assert_logits_close(to_f64(logits), ref, absacc, f"m={m}")
     g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
-    ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K) for r in range(m))
+    gl = to_f64(logits)
+    ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K, gl[r]) for r in range(m))
     assert ties <= max(1, m // 8)
 
 
@@ -263,8 +265,9 @@ def test_tensor_core_topk_adversarial_orders(m, order):
                                 64, n, k, nthreads=16)
     assert_logits_close(to_f64(logits), ref, absacc, order)
     g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
+    gl = to_f64(logits)
     for r in range(m):
-        check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K)
+        check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K, gl[r])
     if order == "equal":
         # every row's logit is the same number: value ties go to the lowest indices
         assert (g_idx == np.arange(K)[None, :]).all(), g_idx[:2]

@@ -132,7 +132,6 @@ extern "C" wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t
     base.counter = counter;
     base.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
     base.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
-    base.gthr = reinterpret_cast<unsigned int*>(ws + lay.gthr_off);
   }
   const size_t esz = 2;
   for (int64_t m0 = 0; m0 < m; m0 += kSliceTokens) {

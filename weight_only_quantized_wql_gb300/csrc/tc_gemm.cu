@@ -22,13 +22,9 @@
 //    mbarriers that release the A / activation buffers and hand finished
 //    accumulators to the epilogue.
 //  * Warps 10..13 (one per TMEM lane quarter) read the accumulator with
-//    tcgen05.ld, add the bias, round to fp16 and store the logits.  For top-K
-//    they pass each 32-token slab through shared memory so that every warp
-//    sees all 128 rows of 8 tokens; a token whose slab holds a value at or
-//    above its running K-th best is merged into that token's list (kept in
-//    shared memory for the CTA's whole row range, owned by one warp).  After
-//    the last tile the lists become this CTA's candidates; a small kernel
-//    (one CTA per token) merges all CTAs' candidates.
+//    tcgen05.ld, add the bias, round to fp16, transpose each 32 x 32 block
+//    through shared memory and store the logits with 16-byte stores.  Top-K
+//    candidates are chosen afterwards from these logits (topk_select.cu).
 //  * Every mbarrier wait is bounded; on a timeout the CTA records an error
 //    in the workspace, skips the remaining work and still frees its TMEM.
 #include <cuda_bf16.h>
@@ -48,9 +44,6 @@ constexpr int kDequantWarps = 8, kEpilogueWarps = 4;
 constexpr int kWChunkBytes = kTileRows * 128;     // one packed-weight chunk (16 KB)
 constexpr int kABytes = kTileRows * 128;          // one 64-column fp16 A block (16 KB)
 constexpr int kWStages = 3, kAStages = 3;
-constexpr int kSlabPitch = 33;                    // floats per slab row (bank spread)
-constexpr int kSlabBytes = (kTileRows * kSlabPitch + 32) * 4;   // 128 rows x 32 tokens, fp32
-constexpr uint32_t kEpilogueBarrier = 3;          // named barrier of the epilogue warps
 constexpr int kStageBytes = kEpilogueWarps * 32 * 32 * 2;   // logits staging, all warps
 
 struct TcParams {
@@ -64,12 +57,11 @@ struct TcParams {
   int xstages;          // activation ring depth when not resident
   int acc_bufs;         // 1 or 2 accumulators in TMEM
   uint32_t tmem_cols;   // power of two >= acc_bufs * npad
-  uint32_t off_w, off_a, off_x, off_bar, off_slab, off_list, off_s;
+  uint32_t off_w, off_a, off_x, off_bar, off_s;
   uint32_t off_st;      // per-epilogue-warp logits staging (32 tokens x 32 rows fp16)
   int vec_store;        // logits rows 16-byte aligned: 16-byte stores allowed
   int sbuf_bytes;       // one tile's scale rows (128 x ngroups halves), 0 = no staging
   int scales_aligned;   // scale table 16-byte aligned
-  int qcap;             // passer-queue entries per token (the queue reuses the slab)
   unsigned int* err;
 };
 
@@ -136,40 +128,6 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void epilogue_sync() {
-  asm volatile("bar.sync %0, %1;" ::"n"(kEpilogueBarrier), "n"(kEpilogueWarps * 32) : "memory");
-}
-
-// Epilogue barrier that also returns whether `v` was true in any epilogue thread.
-__device__ __forceinline__ bool epilogue_any(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "n"(kEpilogueBarrier), "n"(kEpilogueWarps * 32)
-      : "memory");
-  return r != 0u;
-}
-
-// Merge a token's queued candidates into its list (kept sorted in shared
-// memory) and return the new K-th best value.
-template <int KT>
-__device__ __forceinline__ float merge_queue(unsigned long long* tl,
-                                             const unsigned long long* queue, int count, int K) {
-  unsigned long long l[KT];
-#pragma unroll
-  for (int i = 0; i < KT; ++i) l[i] = i < K ? tl[i] : kEmptyKey;
-  for (int i = 0; i < count; ++i) list_insert<KT>(l, queue[i]);
-#pragma unroll
-  for (int i = 0; i < KT; ++i)
-    if (i < K) tl[i] = l[i];
-  const unsigned long long kth = pick(l, K - 1);
-  return kth == kEmptyKey ? -INFINITY : key_value(kth);
-}
-
 // Exact fp16 codes q (pairs in natural order) times the fp16 scale pair s2.
 __device__ __forceinline__ void int4_q_times_s(uint32_t w, uint32_t s2, uint32_t (&out)[4]) {
   uint32_t q[4];
@@ -191,114 +149,11 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// slab element of (row, token): rows 32q..32q+31 are shifted by 8q columns so
-// that both the row-wise writes and the quad-wise reads hit distinct banks.
-__device__ __forceinline__ int slab_index(int row, int tok) {
-  return row * kSlabPitch + tok + 8 * (row >> 5);
-}
-
-// One slab (32 tokens x 128 rows of this tile) against the CTA's running
-// per-token top-K lists.  Warp w owns tokens 8w..8w+7 of the slab, one lane
-// quad per token, lane q of the quad scanning rows 32q..32q+31.  Values below
-// the token's current K-th best cannot enter and are skipped; the quad's
-// leader starts from the token's list, so K rounds of a quad-wide maximum
-// (two shuffles) yield the new list directly.
-template <int KT>
-__device__ __forceinline__ void slab_topk(const float* slab, unsigned long long* lists,
-                                          float* thr, int c0, int t, int m, int n, int K,
-                                          const unsigned int* only) {
-  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) & 3;
-  const int q = lane & 3;
-  const int jl = 8 * w + (lane >> 2);                 // token within the slab
-  const int tok = c0 + jl;
-  const bool live = tok < m && (only == nullptr || only[tok] != 0u);
-  unsigned long long list[KT];
-#pragma unroll
-  for (int i = 0; i < KT; ++i) list[i] = kEmptyKey;
-  int added = 0;
-  // All 32 loads first (independent).  Columns of tokens >= m hold padding
-  // values inside the slab and are read but never used.
-  float v[32];
-  const float* col = slab + slab_index(32 * q, jl);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = col[i * kSlabPitch];
-  const int row0 = t * kTileRows + 32 * q;
-  const int valid = live ? min(32, n - row0) : 0;
-  float t0 = live ? thr[tok] : INFINITY;
-  if (__any_sync(0xFFFFFFFFu, t0 == -INFINITY)) {
-    // A token with no list yet (the CTA's first tile) would insert every
-    // value one by one.  Each lane's R-th largest value, R = KT/4, bounds the
-    // token's K-th best from below -- the quad holds 4R >= K values at least
-    // as large as the smallest of the four -- so values under it are skipped.
-    constexpr int R = KT / 4;
-    float top[R];
-#pragma unroll
-    for (int j = 0; j < R; ++j) top[j] = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float c = i < valid ? v[i] : -INFINITY;
-#pragma unroll
-      for (int j = 0; j < R; ++j) {
-        const float hi = fmaxf(top[j], c);
-        c = fminf(top[j], c);
-        top[j] = hi;
-      }
-    }
-    float lb = top[R - 1];
-    lb = fminf(lb, __shfl_xor_sync(0xFFFFFFFFu, lb, 1));
-    lb = fminf(lb, __shfl_xor_sync(0xFFFFFFFFu, lb, 2));
-    if (t0 == -INFINITY) t0 = lb;
-  }
-  if (live) {
-    if (q == 0) {
-      const unsigned long long* tl = lists + (size_t)tok * KT;
-#pragma unroll
-      for (int i = 0; i < KT; ++i) list[i] = i < K ? tl[i] : kEmptyKey;   // already sorted
-    }
-    uint32_t mask = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) mask |= (i < valid && v[i] >= t0) ? (1u << i) : 0u;
-    added = __popc(mask);
-    while (mask) {
-      const int i = __ffs(mask) - 1;
-      mask &= mask - 1;
-      list_insert<KT>(list, topk_key(col[i * kSlabPitch], (uint32_t)(row0 + i)));
-    }
-  }
-  if (!__any_sync(0xFFFFFFFFu, added > 0)) return;
-  // quads whose lanes added nothing keep their list unchanged
-  const int qa = added + __shfl_xor_sync(0xFFFFFFFFu, added, 1);
-  const bool quad_added = (qa + __shfl_xor_sync(0xFFFFFFFFu, qa, 2)) > 0;
-  const bool writer = live && q == 0 && quad_added;
-  unsigned long long* tl = lists + (size_t)tok * KT;
-  unsigned long long kth = kEmptyKey;
-#pragma unroll
-  for (int r = 0; r < KT; ++r) {
-    if (r < K) {
-      unsigned long long best = list[0];
-      unsigned long long o = shfl_xor_u64(best, 1);
-      best = o > best ? o : best;
-      o = shfl_xor_u64(best, 2);
-      best = o > best ? o : best;
-      if (writer) tl[r] = best;
-      if (r == K - 1) kth = best;
-      if (list[0] == best && best != kEmptyKey) {
-#pragma unroll
-        for (int i = 0; i < KT - 1; ++i) list[i] = list[i + 1];
-        list[KT - 1] = kEmptyKey;
-      }
-    }
-  }
-  if (writer) thr[tok] = kth == kEmptyKey ? -INFINITY : key_value(kth);
-}
-
-// KT: top-K list width compiled in (0 = no top-K code at all, 8 or 16).
-template <int BITS, int KT>
+template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_logits_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
                      const TcParams p) {
   constexpr int kBlocksPerChunk = BITS == 4 ? 4 : 2;   // 64-column blocks per packed chunk
-  constexpr int KL = KT == 0 ? 8 : KT;                 // list width of the (dead) code for KT 0
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -316,12 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_empty = s_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_empty + 2);
   unsigned int* flags = tmem_slot + 1;   // [0] bad
-  float* slab = reinterpret_cast<float*>(sm + p.off_slab);                 // [32][128]
-  unsigned long long* lists = reinterpret_cast<unsigned long long*>(sm + p.off_list);
-  float* thr = reinterpret_cast<float*>(lists + (size_t)p.npad * KL);  // own K-th
-  float* gth = thr + p.npad;                                  // best K-th of any CTA
-  unsigned int* qcnt = reinterpret_cast<unsigned int*>(gth + p.npad);   // queued passers
-  unsigned int* oflow = qcnt + p.npad;                        // queue overflowed this tile
 
   const LogitsArgs& a = p.a;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -352,15 +201,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     flags[0] = 0u;
     fence_barrier_init();
-  }
-  if (a.topk > 0) {
-    for (int i = threadIdx.x; i < p.npad * KL; i += kThreads) lists[i] = kEmptyKey;
-    for (int i = threadIdx.x; i < p.npad; i += kThreads) {
-      thr[i] = i < m ? -INFINITY : INFINITY;   // padding tokens never pass a filter
-      gth[i] = -INFINITY;
-      qcnt[i] = 0u;
-      oflow[i] = 0u;
-    }
   }
   if (warp == kMmaWarp) {
     // tensor-memory accumulators (one warp allocates; freed by the same warp)
@@ -567,28 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ epilogue ------------------------------
     const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
-    const int et = threadIdx.x - kEpilogueWarp0 * 32;   // 0..127
-    const int K = KT == 0 ? 0 : a.topk;
-    unsigned long long* queue = reinterpret_cast<unsigned long long*>(slab);   // fast tiles
+    uint32_t* st = reinterpret_cast<uint32_t*>(sm + p.off_st + quarter * 2048);
+    const bool odd = (lane & 1) != 0;
     int acc = 0;
     uint32_t accph = 0;
     for (int t = T0; t < T1; ++t) {
-      // Top-K mode of this tile.  Until every token has K entries, tiles go
-      // through the slab (full per-token selection).  After that a value can
-      // only enter if it beats the token's K-th best strictly (a later row
-      // loses a tie) and is not below the K-th best any CTA has published;
-      // such rare passers are queued per token and merged after the tile.
-      bool slow = false;
-      if (K > 0) {
-        for (int tok = et; tok < m; tok += kEpilogueWarps * 32) {
-          const float tl = thr[tok];
-          slow |= (tl == -INFINITY);
-          const unsigned int mine = tl == -INFINITY ? 0u : (uint32_t)(topk_key(tl, 0u) >> 32);
-          const unsigned int g = max(atomicMax(a.gthr + tok, mine), mine);
-          gth[tok] = g == 0u ? -INFINITY : key_value((unsigned long long)g << 32);
-        }
-        slow = epilogue_any(slow);
-      }
       if (!bad) bad = !mbar_wait(&acc_full[acc], accph);
       bad = __any_sync(0xFFFFFFFFu, bad);
       tc_fence_after();
@@ -598,137 +421,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                              : 0.f;
       const uint32_t taddr =
           tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * p.npad);
-      // pass 0: logits, and the filter (fast tile) or the slab (slow tile);
-      // pass 1 (fast tile, top-K): merge the queues, then redo through the
-      // slab the tokens whose queue overflowed -- the accumulator is still held
-      for (int pass = 0; pass < 2; ++pass) {
-        if (pass == 1) {
-          if (K == 0 || slow) break;
-          epilogue_sync();                   // every passer is queued
-          bool ovf = false;
-          for (int tok = et; tok < m; tok += kEpilogueWarps * 32) {
-            const unsigned int c = qcnt[tok];
-            if (c == 0u) continue;
-            qcnt[tok] = 0u;
-            if (c > (unsigned int)p.qcap) {
-              oflow[tok] = 1u;
-              ovf = true;
-              continue;
-            }
-            unsigned long long* tl = lists + (size_t)tok * KL;
-            const unsigned long long* tq = queue + (size_t)tok * p.qcap;
-            thr[tok] = merge_queue<KL>(tl, tq, (int)c, K);
-          }
-          if (!epilogue_any(ovf)) break;
+      const int wrow0 = t * kTileRows + quarter * 32;   // first row of this warp
+      for (int c0 = 0; c0 < p.npad && !bad; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + (uint32_t)c0, v);
+        // pair adjacent rows (one shuffle per token pair), stage the warp's
+        // 32 rows x 32 tokens as fp16, then write every token's 64-byte run
+        // of rows with 16-byte stores
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float f0 = __uint_as_float(v[j]) + bias;
+          const float f1 = __uint_as_float(v[j + 1]) + bias;
+          const float recv = __shfl_xor_sync(0xFFFFFFFFu, odd ? f0 : f1, 1);
+          // even lane: token j, rows (lane, lane + 1); odd: token j + 1, rows (lane - 1, lane)
+          const __half2 h = odd ? __floats2half2_rn(recv, f1) : __floats2half2_rn(f0, recv);
+          st[(odd ? j + 1 : j) * 16 + (lane >> 1)] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        const unsigned int* only = pass == 1 ? oflow : nullptr;
-        for (int c0 = 0; c0 < p.npad; c0 += 32) {
-          if (pass == 1) {
-            bool any = false;             // same in every thread (read after a barrier)
-            for (int j = 0; j < 32 && c0 + j < m; ++j) any |= oflow[c0 + j] != 0u;
-            if (!any) continue;
-          }
-          uint32_t v[32];
-          if (!bad) tmem_ld32(taddr + (uint32_t)c0, v);
-          if (pass == 0 && !bad) {
-            // Logits: pair adjacent rows (one shuffle per token pair), stage the
-            // warp's 32 rows x 32 tokens as fp16, then write every token's
-            // 64-byte run of rows with 16-byte stores.
-            uint32_t* st = reinterpret_cast<uint32_t*>(sm + p.off_st + quarter * 2048);
-            const bool odd = (lane & 1) != 0;
+        __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const float f0 = __uint_as_float(v[j]) + bias;
-              const float f1 = __uint_as_float(v[j + 1]) + bias;
-              const float recv = __shfl_xor_sync(0xFFFFFFFFu, odd ? f0 : f1, 1);
-              // even lane: token j, rows (lane, lane + 1); odd: token j + 1, rows (lane - 1, lane)
-              const __half2 h = odd ? __floats2half2_rn(recv, f1) : __floats2half2_rn(f0, recv);
-              st[(odd ? j + 1 : j) * 16 + (lane >> 1)] = *reinterpret_cast<const uint32_t*>(&h);
+        for (int i = 0; i < 4; ++i) {
+          const int id = i * 32 + lane;
+          const int tk = id >> 2, part = id & 3;
+          const int tok = c0 + tk;
+          const int rs = wrow0 + part * 8;
+          const uint4 val = *reinterpret_cast<const uint4*>(st + tk * 16 + part * 4);
+          if (tok < m) {
+            __half* dst = reinterpret_cast<__half*>(a.logits) + (size_t)tok * n + rs;
+            if (p.vec_store && rs + 8 <= n) {
+              *reinterpret_cast<uint4*>(dst) = val;
+            } else {
+              const uint32_t w4[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (rs + e < n)
+                  reinterpret_cast<uint16_t*>(dst)[e] = (uint16_t)(w4[e >> 1] >> (16 * (e & 1)));
             }
-            __syncwarp();
-            const int wrow0 = t * kTileRows + quarter * 32;   // first row of this warp
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int id = i * 32 + lane;
-              const int tk = id >> 2, part = id & 3;
-              const int tok = c0 + tk;
-              const int rs = wrow0 + part * 8;
-              const uint4 val = *reinterpret_cast<const uint4*>(st + tk * 16 + part * 4);
-              if (tok < m) {
-                __half* dst = reinterpret_cast<__half*>(a.logits) + (size_t)tok * n + rs;
-                if (p.vec_store && rs + 8 <= n) {
-                  *reinterpret_cast<uint4*>(dst) = val;
-                } else {
-                  const uint32_t w4[4] = {val.x, val.y, val.z, val.w};
-#pragma unroll
-                  for (int e = 0; e < 8; ++e)
-                    if (rs + e < n)
-                      reinterpret_cast<uint16_t*>(dst)[e] = (uint16_t)(w4[e >> 1] >> (16 * (e & 1)));
-                }
-              }
-            }
-            __syncwarp();
-          }
-          if (pass == 0 && K > 0 && !slow) {
-            if (!bad && row < n) {
-              uint32_t passed = 0;
-#pragma unroll
-              for (int j4 = 0; j4 < 8; ++j4) {
-                const float4 tq = *reinterpret_cast<const float4*>(thr + c0 + 4 * j4);
-                const float4 gq = *reinterpret_cast<const float4*>(gth + c0 + 4 * j4);
-                const float f0 = __uint_as_float(v[4 * j4 + 0]) + bias;
-                const float f1 = __uint_as_float(v[4 * j4 + 1]) + bias;
-                const float f2 = __uint_as_float(v[4 * j4 + 2]) + bias;
-                const float f3 = __uint_as_float(v[4 * j4 + 3]) + bias;
-                passed |= (f0 > tq.x && f0 >= gq.x) ? (1u << (4 * j4 + 0)) : 0u;
-                passed |= (f1 > tq.y && f1 >= gq.y) ? (1u << (4 * j4 + 1)) : 0u;
-                passed |= (f2 > tq.z && f2 >= gq.z) ? (1u << (4 * j4 + 2)) : 0u;
-                passed |= (f3 > tq.w && f3 >= gq.w) ? (1u << (4 * j4 + 3)) : 0u;
-              }
-              const int live_toks = m - c0;   // slab columns past m are padding
-              if (live_toks < 32) passed &= live_toks > 0 ? ((1u << live_toks) - 1u) : 0u;
-              while (passed) {
-                const int j = __ffs(passed) - 1;
-                passed &= passed - 1;
-                uint32_t bits = 0;
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) bits = (jj == j) ? v[jj] : bits;
-                const int tok = c0 + j;
-                const unsigned int pos = atomicAdd(qcnt + tok, 1u);
-                if (pos < (unsigned int)p.qcap)
-                  queue[(size_t)tok * p.qcap + pos] =
-                      topk_key(__uint_as_float(bits) + bias, (uint32_t)row);
-              }
-            }
-          } else if (K > 0) {
-            // slab: this warp's 32 rows of the slab's 32 tokens
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              slab[slab_index(r, j)] = __uint_as_float(v[j]) + bias;
-            epilogue_sync();
-            if (!bad) {
-              slab_topk<KL>(slab, lists, thr, c0, t, m, n, K, only);
-            }
-            epilogue_sync();
           }
         }
-        if (pass == 1)
-          for (int tok = et; tok < m; tok += kEpilogueWarps * 32) oflow[tok] = 0u;
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
       if (++acc == p.acc_bufs) { acc = 0; accph ^= 1u; }
-    }
-    // this CTA's candidates: each epilogue warp writes the lists of its tokens
-    if (K > 0 && !bad) {
-      for (int c0 = 0; c0 < m; c0 += 32)
-        for (int jj = 0; jj < 8; ++jj) {
-          const int tok = c0 + 8 * quarter + jj;
-          if (tok < m && lane < K)
-            a.cand[((size_t)tok * WQL_MAX_CTAS + blockIdx.x) * K + lane] =
-                lists[(size_t)tok * KL + lane];
-        }
     }
   }
 
@@ -744,67 +479,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (flags[0] != 0u && threadIdx.x == 0 && p.err) atomicOr(p.err, 2u);
 }
 
-// Final top-K of one token from every CTA's candidates (one CTA per token).
-template <int KT>
-__global__ void __launch_bounds__(256) topk_merge_kernel(const LogitsArgs a, int nctas,
-                                                         const unsigned int* err) {
-  __shared__ unsigned long long red[8 * KT];
-  const int tok = blockIdx.x, K = a.topk;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool any_bad = __ldcg(err) != 0u;
-  if (threadIdx.x == 0) a.gthr[tok] = 0u;   // ready for the next launch
-  const unsigned long long* src = a.cand + (size_t)tok * WQL_MAX_CTAS * K;
-  unsigned long long list[KT];
-#pragma unroll
-  for (int i = 0; i < KT; ++i) list[i] = kEmptyKey;
-  const int count = any_bad ? 0 : nctas * K;
-  for (int i0 = threadIdx.x; i0 < count; i0 += 8 * 256) {
-    unsigned long long v[8];
-#pragma unroll
-    for (int b = 0; b < 8; ++b)
-      v[b] = i0 + b * 256 < count ? __ldcg(src + i0 + b * 256) : kEmptyKey;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) list_insert<KT>(list, v[b]);
-  }
-  unsigned long long best[KT];
-  warp_merge_topk_redux<KT>(list, K, best);
-  if (lane < KT) red[warp * KT + lane] = pick(best, lane);
-  __syncthreads();
-  if (warp == 0) {
-    unsigned long long l2[KT];
-#pragma unroll
-    for (int i = 0; i < KT; ++i) l2[i] = lane < 8 ? red[lane * KT + i] : kEmptyKey;
-    warp_merge_topk_redux<KT>(l2, K, best);
-    const unsigned long long mine = pick(best, lane);
-    if (lane < K) {
-      const bool ok = !any_bad && mine != kEmptyKey;
-      a.topk_idx[(size_t)tok * K + lane] = ok ? key_index(mine) : -1;
-      a.topk_val[(size_t)tok * K + lane] = ok ? key_value(mine) : __int_as_float(0x7FC00000);
-    }
-  }
-}
-
 struct TcLayout {
-  uint32_t off_w, off_a, off_x, off_bar, off_slab, off_list, off_s, off_st;
+  uint32_t off_w, off_a, off_x, off_bar, off_s, off_st;
   size_t smem;
   int x_resident, xstages, sbuf_bytes;
 };
 
-// Top-K list width compiled into the kernel for a requested top-K.
-int list_width(int topk) { return topk == 0 ? 0 : (topk <= 8 ? 8 : 16); }
-
-// kl: compiled top-K list width (0 = no top-K: no lists, no slab).
-TcLayout tc_plan(int npad, int k, int ngroups, int kl) {
+TcLayout tc_plan(int npad, int k, int ngroups) {
   TcLayout L{};
   const uint32_t xblock = (uint32_t)npad * 128u;
   const int kblocks = k / 64;
-  // per token: list, own K-th, best published K-th, queue count, overflow flag
-  const uint32_t lists = kl > 0 ? (uint32_t)npad * (uint32_t)(kl * 8 + 16) : 0u;
-  const uint32_t slab = kl > 0 ? (uint32_t)kSlabBytes : 0u;
   const uint32_t sbuf = rup((uint32_t)(kTileRows * ngroups * 2), 128u);
   L.sbuf_bytes = (2 * sbuf <= 24u * 1024u) ? (int)sbuf : 0;   // else direct scale loads
-  const uint32_t tail =
-      512 + 128 + slab + 64 + lists + 2 * L.sbuf_bytes + 128 + kStageBytes + 128 + 1024;
+  const uint32_t tail = 512 + 128 + 2 * L.sbuf_bytes + 128 + kStageBytes + 128 + 1024;
   const uint32_t limit = 227u * 1024u;
   uint32_t off = 0;
   L.off_w = off;
@@ -824,10 +511,6 @@ TcLayout tc_plan(int npad, int k, int ngroups, int kl) {
   }
   L.off_bar = rup(off, 64);
   off = L.off_bar + 512;
-  L.off_slab = rup(off, 128);
-  off = L.off_slab + slab;
-  L.off_list = rup(off, 64);
-  off = L.off_list + lists;
   L.off_s = rup(off, 128);
   off = L.off_s + 2 * L.sbuf_bytes;
   L.off_st = rup(off, 128);
@@ -836,10 +519,10 @@ TcLayout tc_plan(int npad, int k, int ngroups, int kl) {
   return L;
 }
 
-template <int BITS, int KT>
+template <int BITS>
 cudaError_t tc_launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p,
                         size_t smem, int ctas, cudaStream_t s) {
-  auto kern = tc_logits_kernel<BITS, KT>;
+  auto kern = tc_logits_kernel<BITS>;
   static size_t configured = 0;
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -858,7 +541,7 @@ bool tc_supported(const LogitsArgs& a) {
   if (a.x_dtype != WQL_F16 || a.scale_dtype != WQL_F16) return false;
   if (a.m < 1 || a.m > 256 || a.k % 64 != 0) return false;
   const int npad = (a.m + 15) / 16 * 16;
-  return tc_plan(npad, a.k, a.k / a.group_eff, list_width(a.topk)).smem <= 227u * 1024u;
+  return tc_plan(npad, a.k, a.k / a.group_eff).smem <= 227u * 1024u;
 }
 
 cudaError_t launch_tc(const LogitsArgs& a, unsigned int* err, cudaStream_t s) {
@@ -876,7 +559,7 @@ cudaError_t launch_tc(const LogitsArgs& a, unsigned int* err, cudaStream_t s) {
   uint32_t cols = 32;
   while (cols < (uint32_t)(p.acc_bufs * p.npad)) cols <<= 1;
   p.tmem_cols = cols;
-  const TcLayout L = tc_plan(p.npad, a.k, p.ngroups, list_width(a.topk));
+  const TcLayout L = tc_plan(p.npad, a.k, p.ngroups);
   p.sbuf_bytes = L.sbuf_bytes;
   p.off_s = L.off_s;
   p.scales_aligned = (reinterpret_cast<uintptr_t>(a.scales) % 16) == 0;
@@ -886,13 +569,8 @@ cudaError_t launch_tc(const LogitsArgs& a, unsigned int* err, cudaStream_t s) {
   p.off_a = L.off_a;
   p.off_x = L.off_x;
   p.off_bar = L.off_bar;
-  p.off_slab = L.off_slab;
-  p.off_list = L.off_list;
   p.off_st = L.off_st;
   p.vec_store = (a.n % 8 == 0) && (reinterpret_cast<uintptr_t>(a.logits) % 16 == 0);
-  // the passer queue lives in the slab: as many whole entries per token as fit
-  p.qcap = (int)((kSlabBytes / 8) / (uint32_t)p.npad);
-  if (p.qcap > 32) p.qcap = 32;
 
   CUtensorMap tw, tx;
   cudaError_t e = make_tmap_2d(&tw, a.qweight, 4, (uint64_t)row_bytes / 4, (uint64_t)a.n,
@@ -905,22 +583,8 @@ cudaError_t launch_tc(const LogitsArgs& a, unsigned int* err, cudaStream_t s) {
   int ctas = device_sm_count();
   if (ctas > p.tiles_total) ctas = p.tiles_total;
   if (ctas > WQL_MAX_CTAS) ctas = WQL_MAX_CTAS;
-  if (a.topk == 0)
-    e = a.bits == 4 ? tc_launch_t<4, 0>(tw, tx, p, L.smem, ctas, s)
-                    : tc_launch_t<8, 0>(tw, tx, p, L.smem, ctas, s);
-  else if (a.topk <= 8)
-    e = a.bits == 4 ? tc_launch_t<4, 8>(tw, tx, p, L.smem, ctas, s)
-                    : tc_launch_t<8, 8>(tw, tx, p, L.smem, ctas, s);
-  else
-    e = a.bits == 4 ? tc_launch_t<4, 16>(tw, tx, p, L.smem, ctas, s)
-                    : tc_launch_t<8, 16>(tw, tx, p, L.smem, ctas, s);
-  if (e != cudaSuccess || a.topk <= 0) return e;
-  if (a.topk <= 8)
-    topk_merge_kernel<8><<<a.m, 256, 0, s>>>(a, ctas, err);
-  else
-    topk_merge_kernel<16><<<a.m, 256, 0, s>>>(a, ctas, err);
-  note_launch();
-  return cudaGetLastError();
+  return a.bits == 4 ? tc_launch_t<4>(tw, tx, p, L.smem, ctas, s)
+                     : tc_launch_t<8>(tw, tx, p, L.smem, ctas, s);
 }
 
 }  // namespace wql

@@ -90,7 +90,8 @@ WorkspaceLayout workspace_layout(int64_t m, int64_t n, int32_t topk) {
   WorkspaceLayout l{};
   l.counter_off = 0;
   size_t off = 256;
-  l.gthr_off = off;
+  // fixed place (any m): per-token tickets of the top-K selection
+  l.tickets_off = off;
   if (topk > 0) off += 256 * sizeof(unsigned int);
   l.cand_off = off;
   if (topk > 0) off += round_up((size_t)m * WQL_MAX_CTAS * (size_t)topk * 8, 256);
@@ -232,7 +233,7 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
     base.counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
     base.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
     base.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
-    base.gthr = reinterpret_cast<unsigned int*>(ws + lay.gthr_off);
+    base.tickets = reinterpret_cast<unsigned int*>(ws + lay.tickets_off);
   }
   // Token counts above 16 go to the tensor-core kernel (up to 256 tokens per
   // launch) when it supports the dtype combination; otherwise the decode
@@ -252,9 +253,13 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
       a.topk_val = topk_val + (size_t)m0 * topk;
     }
     cudaError_t e;
-    if (use_tc && mc > kDecodeMaxTokens)
-      e = launch_tc(a, err_word, stream);
-    else
+    if (use_tc && mc > kDecodeMaxTokens) {
+      // logits on the tensor cores, then the top-K from the rounded logits
+      LogitsArgs g = a;
+      g.topk = 0;
+      e = launch_tc(g, err_word, stream);
+      if (e == cudaSuccess && a.topk > 0) e = launch_topk_select(a, stream);
+    } else
       e = launch_decode(a, err_word, stream);
     if (e != cudaSuccess) return cuda_fail(e);
   }

@@ -426,16 +426,20 @@ struct LogitsArgs {
   unsigned int* counter;      // zero between calls; the last CTA resets it
   unsigned long long* cand;   // [m][WQL_MAX_CTAS][topk] keys
   float* scratch;             // [m][n] fp32 logits (top-K input, decode path)
-  unsigned int* gthr;         // [256] per-token K-th best seen by any CTA, orderable
-                              // bits (0 = none); zero between calls (tensor-core path)
+  unsigned int* tickets;      // [256] per-token tickets of the top-K selection
+                              // (zero between calls)
 };
 // Bandwidth-bound path for m <= 16 (TMA-fed warp MMA, split over vocab rows).
 // `err` is the workspace's sticky error word.
 cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s);
 size_t decode_smem_bytes(int m, int k, int bits, int group_eff);
-// Tensor-core path for 16 < m <= 256 (fp16 activations and scales).
+// Tensor-core path for 16 < m <= 256 (fp16 activations and scales): logits
+// only (a.topk is ignored; launch_topk_select follows it).
 bool tc_supported(const LogitsArgs& a);
 cudaError_t launch_tc(const LogitsArgs& a, unsigned int* err, cudaStream_t s);
+// Top-K of each token row from the rounded logits already written to
+// a.logits, candidates recomputed in fp32 from the packed weight.
+cudaError_t launch_topk_select(const LogitsArgs& a, cudaStream_t s);
 
 struct RescoreArgs {
   const void* x;
@@ -452,7 +456,7 @@ cudaError_t launch_rescore(const RescoreArgs& a, cudaStream_t s);
 
 // Workspace layout shared by the launchers and wql_workspace_size().
 struct WorkspaceLayout {
-  size_t counter_off, gthr_off, cand_off, scratch_off, total;
+  size_t counter_off, tickets_off, cand_off, scratch_off, total;
 };
 WorkspaceLayout workspace_layout(int64_t m, int64_t n, int32_t topk);
 
