@@ -178,6 +178,7 @@ constexpr int kStages = 5;                       // stages in flight (80 KB per 
 
 struct SelShared {
   uint64_t bar[kStages];                    // stage ring (bulk copies of the row)
+  unsigned int cons[kStages];               // warps done with a stage's current fill
   unsigned int bad;                         // a bounded wait timed out
   Hist H;
   unsigned int count, thresh, last, nbest, nlive;
@@ -317,13 +318,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const LogitsAr
   const int need = min(K, hi - lo);
   const uint16_t* row = reinterpret_cast<const uint16_t*>(a.logits) + (size_t)tok * n;
   const bool vec = (n % kPer == 0) && (reinterpret_cast<uintptr_t>(a.logits) % 16 == 0);
-  {
-    // the token's activations, for the recompute
-    const uint4* xg = reinterpret_cast<const uint4*>(reinterpret_cast<const XT*>(a.x) +
-                                                     (size_t)tok * a.k);
-    for (int i = threadIdx.x; i < a.k / 8; i += kThreads)
-      reinterpret_cast<uint4*>(xs)[i] = __ldg(xg + i);
-  }
   if (threadIdx.x == 0) {
     S.count = 0u;
     S.thresh = 0u;
@@ -396,44 +390,71 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const LogitsAr
       bulk_load(ring + (size_t)(st % kStages) * kStepBytes, row + start, bytes,
                 &S.bar[st % kStages]);
     };
-    int issued = 0;                        // thread 0: steps whose copy was issued
     if (threadIdx.x == 0) {
-      for (int b = 0; b < kStages; ++b) mbar_init(&S.bar[b], 1);
+      for (int b = 0; b < kStages; ++b) {
+        mbar_init(&S.bar[b], 1);
+        S.cons[b] = 0u;
+      }
       fence_barrier_init();
       S.bad = 0u;
-      for (; issued < kStages && issued < nsteps; ++issued) issue(issued);
+      for (int st = 0; st < kStages && st < nsteps; ++st) issue(st);
+    }
+    // the token's activations, for the recompute (loaded while the first
+    // copies are in flight)
+    {
+      const uint4* xg = reinterpret_cast<const uint4*>(reinterpret_cast<const XT*>(a.x) +
+                                                       (size_t)tok * a.k);
+      for (int i = threadIdx.x; i < a.k / 8; i += kThreads)
+        reinterpret_cast<uint4*>(xs)[i] = __ldg(xg + i);
     }
     __syncthreads();
     unsigned int t2 = 0u;
-    int st = 0;
-    for (; st < nsteps; ++st) {
-      if (!mbar_wait(&S.bar[st % kStages], (uint32_t)((st / kStages) & 1))) S.bad = 1u;
+    for (int st = 0; st < nsteps; ++st) {
+      const int b = st % kStages;
+      if (!mbar_wait(&S.bar[b], (uint32_t)((st / kStages) & 1))) S.bad = 1u;
       uint4 cur[kLoads];
-      const uint4* src = reinterpret_cast<const uint4*>(ring + (size_t)(st % kStages) * kStepBytes);
+      const uint4* src = reinterpret_cast<const uint4*>(ring + (size_t)b * kStepBytes);
 #pragma unroll
       for (int l = 0; l < kLoads; ++l) cur[l] = src[l * kThreads + threadIdx.x];
       if (st == 0) {
-        thresh = first_threshold(cur);
+        thresh = first_threshold(cur);     // all warps meet here once
         t2 = (thresh & 0x7FFFu) * 0x10001u;
       }
+      // the step's data is in registers: release the stage; the last warp
+      // to release it refills it (no block-wide barrier per step)
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        if (atomicAdd(&S.cons[b], 1u) == (unsigned int)(kWarps - 1)) {
+          S.cons[b] = 0u;
+          if (st + kStages < nsteps) issue(st + kStages);
+        }
+      }
       queue_step(lo + st * kStep, thresh, t2, cur);
-      __syncthreads();                     // the stage is free again
-      if (S.bad != 0u) break;
-      if (threadIdx.x == 0 && st + kStages < nsteps) issue(issued++);
     }
+    __syncthreads();
     if (S.bad != 0u) {
       // a copy did not arrive in time (a stalled GPU): record it in the
-      // error word, wait (bounded) for the copies still in flight, and
-      // report nothing for this range
+      // error word, wait (bounded) for every stage's last fill, and report
+      // nothing for this range
       if (threadIdx.x == 0) {
         atomicOr(a.counter + 1, 4u);
-        for (int k2 = st + 1; k2 < issued; ++k2)
-          mbar_wait(&S.bar[k2 % kStages], (uint32_t)((k2 / kStages) & 1));
+        for (int b = 0; b < kStages && b < nsteps; ++b) {
+          const int last = b + (nsteps - 1 - b) / kStages * kStages;
+          mbar_wait(&S.bar[b], (uint32_t)((last / kStages) & 1));
+        }
         S.count = 0u;
       }
       __syncthreads();
     }
   } else {
+    // the token's activations, for the recompute
+    {
+      const uint4* xg = reinterpret_cast<const uint4*>(reinterpret_cast<const XT*>(a.x) +
+                                                       (size_t)tok * a.k);
+      for (int i = threadIdx.x; i < a.k / 8; i += kThreads)
+        reinterpret_cast<uint4*>(xs)[i] = __ldg(xg + i);
+    }
     // rows not 16-byte aligned: register loads, the next step's issued
     // before the current one is compared
     uint4 cur[kLoads];
