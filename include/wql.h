@@ -136,8 +136,16 @@ size_t wql_workspace_size(int64_t m, int64_t n, int32_t topk);
  *              nearest-even in x_dtype
  *   topk       0 (no candidates) or 1..WQL_MAX_TOPK, topk <= n
  *   topk_idx   device int32 [m, topk] (NULL when topk == 0)
- *   topk_val   device float [m, topk]: the fp32 logits before output
- *              rounding, ordered by value descending, then index ascending
+ *   topk_val   device float [m, topk]: fp32 logits, ordered by value
+ *              descending, then index ascending.  For m <= 16 they are the
+ *              fp32 accumulators that logits_out rounds.  For m > 16 the
+ *              tensor-core kernel folds each group's scale into fp16 weights
+ *              (q * s rounded to fp16); the candidates are then the rows whose
+ *              rounded logit is at least the K-th largest rounded logit, and
+ *              their values are recomputed in fp32 from the packed weight
+ *              (exact q * x products, one fp32 sum per group, times the
+ *              group's scale).  The two can differ by the folding rounding
+ *              (at most 2^-11 relative per weight).
  *   workspace  device, ws_bytes >= wql_workspace_size(m, n, topk)
  * The kernel is chosen from m inside the library. */
 wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m,
