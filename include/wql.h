@@ -146,7 +146,10 @@ size_t wql_workspace_size(int64_t m, int64_t n, int32_t topk);
  *              (exact q * x products, one fp32 sum per group, times the
  *              group's scale).  The two can differ by the folding rounding
  *              (at most 2^-11 relative per weight).
- *   workspace  device, ws_bytes >= wql_workspace_size(m, n, topk)
+ *   workspace  device, 256-byte aligned, ws_bytes >= wql_workspace_size(m, n,
+ *              topk); may be NULL when topk == 0 (the decode kernel then
+ *              splits the vocab rows evenly instead of handing work units
+ *              out through the workspace's counter)
  * The kernel is chosen from m inside the library. */
 wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m,
                       const wql_weight* w, const void* bias, void* logits_out,
@@ -173,8 +176,9 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m,
  *     area's device address with that device current); make that first call
  *     before any stream capture begins.  A failed setup returns WQL_ECUDA and
  *     is retried by the next call.
- *   - The area's ticket counter and error word are cleared on `stream` at
- *     the start of every call (one small memset before the launches).
+ *   - The area's first 256 bytes (ticket counter, error word, per-token
+ *     top-K bounds) are cleared on `stream` at the start of every call (one
+ *     small memset before the launches).
  *   - Calls on one device share the area: calls that may be in flight at
  *     the same time (other streams, unsynchronised host threads) race and
  *     corrupt each other's outputs.  Serialise them.

@@ -244,13 +244,14 @@ def _rowwise_weight(n, k, row_value):
     return vals[:, None].expand(n, k).contiguous()
 
 
-@pytest.mark.parametrize("m", [32, 256])
+@pytest.mark.parametrize("m", [1, 4, 32, 256])
 @pytest.mark.parametrize("order", ["increasing", "decreasing", "equal"])
 def test_tensor_core_topk_adversarial_orders(m, order):
-    """Logits that grow with the row index make every tile beat every
-    threshold (per-token queues overflow and the tile is redone through the
-    full selection); equal logits must give the lowest indices; decreasing
-    logits never pass after the first tile."""
+    """Logits that grow with the row index put the best rows last; decreasing
+    ones put them first; equal logits must give the lowest indices, and every
+    row ties with the threshold, so the thresholded candidate lists overflow
+    and the exhaustive selection runs (decode kernel for m <= 16, selection
+    kernel after the tensor-core kernel above)."""
     n, k, K = 40000, 128, 8
     f = {"increasing": lambda r: 0.01 + 1e-5 * r, "decreasing": lambda r: 0.5 - 1e-5 * r,
          "equal": lambda r: 0.02}[order]

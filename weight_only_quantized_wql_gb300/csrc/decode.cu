@@ -20,11 +20,16 @@ using decode_detail::round_up_u32;
 
 struct Layout {
   int chunks, ngroups, nsb, sbuf_bytes, xbox_bytes, x_resident;
-  uint32_t off_x, off_s, off_corr, off_bar, off_red;
+  uint32_t off_x, off_s, off_corr, off_bar, off_red, off_blk, off_vals;
+  int vals_stride;
   size_t smem;
 };
 
-Layout plan(int m, int k, int bits, int group_eff, bool allow_resident) {
+// vals_rows > 0: room for the fp32 logits of that many rows per token (the
+// top-K input), with a row stride of 4 mod 32 words so that the epilogue's
+// stores of one instruction fall in distinct banks.
+Layout plan(int m, int k, int bits, int group_eff, bool allow_resident, int cap_units,
+            int vals_rows) {
   Layout L{};
   const int row_bytes = k * bits / 8;
   const int units = bits == 4 ? 4 : 2;
@@ -46,17 +51,61 @@ Layout plan(int m, int k, int bits, int group_eff, bool allow_resident) {
   off = L.off_bar + 2 * kStages * 8 + 16;
   L.off_red = round_up_u32(off, 64);
   off = L.off_red + kWarpsAll * WQL_MAX_TOPK * 8;
+  L.off_blk = round_up_u32(off, 16);
+  off = L.off_blk + (uint32_t)(kStages + cap_units) * 4u;
+  if (vals_rows > 0) {
+    L.vals_stride = (int)round_up_u32((uint32_t)vals_rows, 32u) + 4;
+    L.off_vals = round_up_u32(off, 16);
+    off = L.off_vals + (uint32_t)m * (uint32_t)L.vals_stride * 4u;
+  }
   L.smem = off + 1024;   // slack for aligning the base to 1024
   return L;
 }
 
 constexpr size_t kSmemLimit = 227 * 1024;
 
-Layout choose(int m, int k, int bits, int group_eff) {
-  Layout L = plan(m, k, bits, group_eff, true);
-  if (L.smem <= kSmemLimit) return L;
-  return plan(m, k, bits, group_eff, false);
+// Preference: resident activations first (they serve the whole main loop),
+// then the top-K logits in shared memory rather than a global scratch row.
+Layout choose(int m, int k, int bits, int group_eff, int cap_units, int vals_rows) {
+  Layout L{};
+  for (int res = 1; res >= 0; --res) {
+    if (vals_rows > 0) {
+      L = plan(m, k, bits, group_eff, res != 0, cap_units, vals_rows);
+      if (L.smem <= kSmemLimit) return L;
+    }
+    L = plan(m, k, bits, group_eff, res != 0, cap_units, 0);
+    if (L.smem <= kSmemLimit) return L;
+  }
+  return L;
 }
+
+// Work split.  A unit is up to kBlockTiles 16-row tiles (one TMA box per
+// chunk when full); smaller units when there are too few for about three per
+// CTA.  CTAs take units from a counter in the workspace, so those whose
+// copies stream faster take more; cap_units bounds one CTA's share (room for
+// its unit list and top-K rows) and is never below an even share.
+struct Split {
+  int ctas, unit_tiles, units_total, cap_units;
+};
+
+Split split_work(int tiles_total, bool dynamic) {
+  Split w{};
+  int ctas = device_sm_count();
+  if (ctas > WQL_MAX_CTAS) ctas = WQL_MAX_CTAS;
+  if (ctas < 1) ctas = 1;
+  int u = kBlockTiles;
+  if (tiles_total < 3 * kBlockTiles * ctas) u = (tiles_total + 3 * ctas - 1) / (3 * ctas);
+  if (u < 1) u = 1;
+  w.unit_tiles = u;
+  w.units_total = (tiles_total + u - 1) / u;
+  w.ctas = ctas < w.units_total ? ctas : w.units_total;
+  const int even = (w.units_total + w.ctas - 1) / w.ctas;
+  w.cap_units = dynamic ? (2 * even < 64 ? 2 * even : (even > 64 ? even : 64)) : even;
+  return w;
+}
+
+// the shared-memory need does not depend on the split beyond the unit list
+constexpr int kPlanCapUnits = 64;
 
 }  // namespace
 
@@ -73,16 +122,27 @@ extern template cudaError_t dispatch_x<__nv_bfloat16>(const CUtensorMap&, const 
 }  // namespace decode_detail
 
 size_t decode_smem_bytes(int m, int k, int bits, int group_eff) {
-  return choose(m, k, bits, group_eff).smem;
+  return choose(m, k, bits, group_eff, kPlanCapUnits, 0).smem;
 }
 
 cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s) {
-  const Layout L = choose(a.m, a.k, a.bits, a.group_eff);
+  const int tiles_total = (a.n + 15) / 16;
+  const bool dynamic = a.counter != nullptr;
+  const Split w = split_work(tiles_total, dynamic);
+  const int ctas = w.ctas;
+  // a CTA's top-K rows: at most cap_units units of unit_tiles tiles
+  const int rows_cta = a.topk > 0 ? w.cap_units * w.unit_tiles * 16 : 0;
+  const Layout L = choose(a.m, a.k, a.bits, a.group_eff, w.cap_units, rows_cta);
   if (L.smem > kSmemLimit || a.m > kMaxTok) return cudaErrorInvalidConfiguration;
   decode_detail::DecodeParams p{};
   p.a = a;
   p.err = err;
-  p.tiles_total = (a.n + 15) / 16;
+  p.tiles_total = tiles_total;
+  p.unit_tiles = w.unit_tiles;
+  p.units_total = w.units_total;
+  p.cap_units = w.cap_units;
+  p.sched = dynamic ? a.counter + 2 : nullptr;
+  p.off_blk = L.off_blk;
   p.chunks = L.chunks;
   p.gunits = a.group_eff / 64;
   p.ngroups = L.ngroups;
@@ -96,6 +156,8 @@ cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s
   p.off_corr = L.off_corr;
   p.off_bar = L.off_bar;
   p.off_red = L.off_red;
+  p.off_vals = L.off_vals;
+  p.vals_stride = L.vals_stride;
 
   const int row_bytes = a.k * a.bits / 8;
   CUtensorMap tw, twb, tx;
@@ -109,10 +171,6 @@ cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s
                    (uint32_t)a.m, Swizzle::k128B);
   if (e != cudaSuccess) return e;
 
-  int ctas = device_sm_count();
-  if (ctas > p.tiles_total) ctas = p.tiles_total;
-  if (ctas > WQL_MAX_CTAS) ctas = WQL_MAX_CTAS;
-  if (ctas < 1) ctas = 1;
   if (a.x_dtype == WQL_F16)
     return decode_detail::dispatch_x<__half>(tw, twb, tx, p, L.smem, ctas, s);
   return decode_detail::dispatch_x<__nv_bfloat16>(tw, twb, tx, p, L.smem, ctas, s);

@@ -7,12 +7,16 @@
 // item 1: at M = 1 only the bytes moved matter).
 //
 // Design (sm_103a, one persistent CTA per SM):
-//  * The CTA owns a contiguous range of 16-row vocab tiles, walked in blocks
-//    of up to 256 rows.  Each block streams along the hidden dimension in
-//    chunks of 128 packed bytes per row (256 int4 or 128 int8 codes).
+//  * Work comes in units of up to 16 16-row vocab tiles (256 rows).  A CTA
+//    starts with the unit of its own index and takes further ones from a
+//    counter in the workspace, so CTAs whose copies stream faster take more
+//    (static strided units when there is no workspace).  Each unit streams
+//    along the hidden dimension in chunks of 128 packed bytes per row (256
+//    int4 or 128 int8 codes).
 //  * Warp 16 is the producer: one lane issues TMA tensor copies of every
-//    chunk (16-row boxes, 128B-swizzled) and, once per block, a bulk copy of
-//    the block's scale rows, into a 4-stage ring.  Activations are either
+//    chunk (16-row boxes, 128B-swizzled) and, once per unit, a bulk copy of
+//    the unit's scale rows, into a 4-stage ring; each stage carries its unit
+//    id, and a last stage with id -1 tells the consumers to stop.  Activations are either
 //    resident in shared memory for the whole launch or, when m*k is too
 //    large for that, copied per chunk with the weights.
 //  * Warps 0..15 are consumers, one 16-row tile each.  ldmatrix moves packed
@@ -22,9 +26,13 @@
 //    exact products and fp32 accumulation, and offset * sum(x) -- computed
 //    once per launch for every (token, group) -- is subtracted per scale
 //    group before the exact fp32 scale multiply.
-//  * Top-K: fp32 logits go to a scratch row; each CTA selects its own rows'
-//    top-K per token (all warps, token x row-slice), and the last CTA to
-//    finish (atomic ticket, no waiting) merges all CTAs' candidates.
+//  * Top-K: the fp32 logits of the CTA's rows go to shared memory (or, when
+//    they do not fit, a global scratch row).  Each CTA takes a threshold per
+//    token -- the K-th largest of each warp's lane maxima, a lower bound of
+//    the K-th largest value -- keeps the rows at or above it and selects its
+//    top-K from those; it also raises a per-token global bound with its K-th
+//    value.  The last CTA to finish (atomic ticket, no waiting) keeps the
+//    CTAs' candidates at or above that bound and selects the final top-K.
 //  * All mbarrier waits are bounded; a timeout sets the workspace error word
 //    and the CTA finishes without issuing further copies.
 #pragma once
@@ -48,10 +56,17 @@ constexpr int kStageWBytes = kBlockTiles * kTileBytes;
 constexpr int kStages = 4;
 constexpr int kMaxTok = 16;
 constexpr int kConsumerBarrier = 1;              // named barrier for the consumer warps
+constexpr int kSelCap = 256;                     // candidate slots per token in the selection
+constexpr int kTauWord = 16;                     // workspace word of token 0's global bound
 
 struct DecodeParams {
   LogitsArgs a;
   int tiles_total;      // ceil(n / 16)
+  int unit_tiles;       // 16-row tiles per work unit (<= kBlockTiles)
+  int units_total;      // ceil(tiles_total / unit_tiles)
+  int cap_units;        // most units one CTA takes (cap_units * grid >= units_total)
+  unsigned int* sched;  // [0] next unit - grid, [1] CTAs done; null: static units
+  uint32_t off_blk;     // int unit id per ring stage, then the CTA's unit ids in order
   int chunks;           // chunks per row
   int gunits;           // 64-column units per scale group
   int ngroups;          // scale groups per row
@@ -60,8 +75,19 @@ struct DecodeParams {
   uint32_t off_x, off_s, off_corr, off_bar, off_red;
   int sbuf_bytes, nsb;  // scale buffer size and count
   int scales_aligned;   // scale table 16-byte aligned (bulk copies allowed)
+  uint32_t off_vals;    // fp32 logits of the CTA's rows for the top-K, [token][vals_stride]
+  int vals_stride;      // 0: no room in shared memory, the global scratch row is used
   unsigned int* err;    // sticky error word in the workspace (null: none)
 };
+
+// Working area of the top-K selection.  It lives in the weight ring, which is
+// free once the main loop has consumed every stage.
+struct SelWork {
+  unsigned int thr[kMaxTok];                   // value-key threshold per token
+  unsigned int cnt[kMaxTok];                   // entries kept per token
+  unsigned long long cand[kMaxTok][kSelCap];   // the kept keys
+};
+static_assert(sizeof(SelWork) <= (size_t)kStages * kStageWBytes, "selection area > ring");
 
 __host__ __device__ constexpr uint32_t round_up_u32(uint32_t v, uint32_t a) {
   return (v + a - 1) / a * a;
@@ -113,26 +139,135 @@ __device__ __forceinline__ void select_topk(int m, int K, int count, unsigned lo
   }
 }
 
-// This CTA's candidates, the ticket, and (last CTA only) the final merge.
-template <int KT, typename XT>
-__device__ __forceinline__ void topk_tail(const LogitsArgs& a, unsigned int* err,
-                                          unsigned long long* red, unsigned int* flags,
-                                          int row_begin, int row_end, bool cta_bad) {
+// The K-th largest of the 32 lanes' values (0 if fewer than K are non-zero):
+// K rounds of a warp maximum, each removing one lane that holds it.
+template <int KT>
+__device__ __forceinline__ uint32_t warp_kth_u32(uint32_t v, int K) {
   const int lane = threadIdx.x & 31;
+  uint32_t kth = 0u;
+#pragma unroll
+  for (int r = 0; r < KT; ++r) {
+    if (r < K) {
+      const uint32_t mm = redux_max_u32(v);
+      kth = mm;
+      const unsigned int tied = __ballot_sync(0xFFFFFFFFu, v == mm);
+      if (lane == __ffs(tied) - 1) v = 0u;
+    }
+  }
+  return kth;
+}
+
+// Threshold selection of the top-K keys of entries [0, count) per token, by
+// all threads of the CTA.  W.thr[t] must hold a lower bound of token t's K-th
+// largest value key (0 if none) and W.cnt[t] zero, visible to all threads.
+// With kScan the CTA first raises each bound to the K-th largest of every
+// warp's lane maxima: K lanes hold disjoint entries at or above it, so it
+// does not exceed the token's K-th largest value.  The entries whose value
+// key reaches the bound are kept (all of the top K are among them) and warp
+// w < m selects token w's top K from those (out_tok = w; others -1).
+// Returns false, with nothing selected, if a token kept more than kSelCap
+// entries (many equal values); the caller then selects exhaustively.
+template <int KT, bool kScan, typename Load>
+__device__ __forceinline__ bool cta_topk(int m, int K, int count, Load load, SelWork& W,
+                                         unsigned long long (&out)[KT], int& out_tok) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int slices = max(1, kWarpsAll / m);
+  const bool worker = warp < slices * m;
+  const int tok = warp % m, sl = warp / m;
+  const int step = slices * 32;
+  if (kScan) {
+    if (worker) {
+      uint32_t mx = 0u;
+      for (int i0 = sl * 32 + lane; i0 < count; i0 += 8 * step) {
+        unsigned long long v[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const int i = i0 + b * step;
+          v[b] = i < count ? load(tok, i) : kEmptyKey;
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) mx = max(mx, (uint32_t)(v[b] >> 32));
+      }
+      const uint32_t kth = warp_kth_u32<KT>(mx, K);
+      if (lane == 0 && kth > 0u) atomicMax(&W.thr[tok], kth);
+    }
+    __syncthreads();
+  }
+  if (worker) {
+    const uint32_t th = W.thr[tok];
+    for (int i0 = sl * 32 + lane; i0 < count; i0 += 8 * step) {
+      unsigned long long v[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int i = i0 + b * step;
+        v[b] = i < count ? load(tok, i) : kEmptyKey;
+      }
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (v[b] != kEmptyKey && (uint32_t)(v[b] >> 32) >= th) {
+          const unsigned int at = atomicAdd(&W.cnt[tok], 1u);
+          if (at < (unsigned int)kSelCap) W.cand[tok][at] = v[b];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  bool overflow = false;
+  for (int t = 0; t < m; ++t) overflow |= W.cnt[t] > (unsigned int)kSelCap;
+  out_tok = -1;
+  if (overflow) return false;
+  if (warp < m) {
+    const int c = (int)W.cnt[warp];
+    unsigned long long list[KT];
+#pragma unroll
+    for (int i = 0; i < KT; ++i) list[i] = kEmptyKey;
+    for (int i = lane; i < c; i += 32) list_insert<KT>(list, W.cand[warp][i]);
+    warp_merge_topk_redux<KT>(list, K, out);
+    out_tok = warp;
+  }
+  return true;
+}
+
+// This CTA's candidates, the ticket, and (last CTA only) the final merge.
+// The CTA's rows are its nunits work units in the order it took them
+// (unit ids in blk_list); entry i is row blk_list[i / R] * R + i % R with R
+// the rows per unit.  svals: their fp32 logits in shared memory
+// ([token][vals_stride], entry order), or null for the global scratch row.
+template <int KT, typename XT>
+__device__ __forceinline__ void topk_tail(const DecodeParams& p, SelWork& W,
+                                          unsigned long long* red, unsigned int* flags,
+                                          int nunits, const int* blk_list, bool cta_bad,
+                                          const float* svals) {
+  const LogitsArgs& a = p.a;
+  unsigned int* err = p.err;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int m = a.m, n = a.n, K = a.topk;
+  unsigned int* tau = a.counter + kTauWord;   // per-token bound on the K-th value key
   if (!cta_bad) {
+    const int R = p.unit_tiles * 16;
+    const int count = nunits * R;
+    const int vs = p.vals_stride;
+    auto load = [&](int tk, int i) -> unsigned long long {
+      const int li = i / R;
+      const int row = blk_list[li] * R + (i - li * R);
+      if (row >= n) return kEmptyKey;
+      const float v = svals ? svals[tk * vs + i] : __ldcg(a.scratch + (size_t)tk * n + row);
+      return topk_key(v, (uint32_t)row);
+    };
+    if (threadIdx.x < m) {
+      W.thr[threadIdx.x] = 0u;
+      W.cnt[threadIdx.x] = 0u;
+    }
+    __syncthreads();
     unsigned long long best[KT];
     int tok;
-    select_topk<KT>(
-        m, K, row_end - row_begin, red,
-        [&](int tk, int i) {
-          const int r = row_begin + i;
-          return topk_key(__ldcg(a.scratch + (size_t)tk * n + r), (uint32_t)r);
-        },
-        best, tok);
+    if (!cta_topk<KT, true>(m, K, count, load, W, best, tok))
+      select_topk<KT>(m, K, count, red, load, best, tok);
     if (tok >= 0) {
       const unsigned long long mine = pick(best, lane);
       if (lane < K) a.cand[((size_t)tok * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
+      const unsigned long long kth = pick(best, K - 1);
+      if (lane == 0 && kth != kEmptyKey) atomicMax(tau + tok, (uint32_t)(kth >> 32));
       __threadfence();
     }
   }
@@ -147,11 +282,23 @@ __device__ __forceinline__ void topk_tail(const LogitsArgs& a, unsigned int* err
   __threadfence();
   const bool any_bad = (__ldcg(err) != 0u);
   unsigned long long best[KT];
-  int tok;
-  select_topk<KT>(
-      m, K, any_bad ? 0 : (int)gridDim.x * K, red,
-      [&](int tk, int i) { return __ldcg(a.cand + (size_t)tk * WQL_MAX_CTAS * K + i); }, best,
-      tok);
+  int tok = -1;
+  if (!any_bad) {
+    // every CTA's K-th value bounds the final K-th value from below
+    const int count = (int)gridDim.x * K;
+    auto load = [&](int tk, int i) { return __ldcg(a.cand + (size_t)tk * WQL_MAX_CTAS * K + i); };
+    if (threadIdx.x < m) {
+      W.thr[threadIdx.x] = __ldcg(tau + threadIdx.x);
+      W.cnt[threadIdx.x] = 0u;
+    }
+    __syncthreads();
+    if (!cta_topk<KT, false>(m, K, count, load, W, best, tok))
+      select_topk<KT>(m, K, count, red, load, best, tok);
+  } else if (warp < m) {
+    tok = warp;   // an internal wait timed out somewhere: report no entries
+#pragma unroll
+    for (int i = 0; i < KT; ++i) best[i] = kEmptyKey;
+  }
   if (tok >= 0) {
     const unsigned long long mine = pick(best, lane);
     if (lane < K) {
@@ -161,7 +308,25 @@ __device__ __forceinline__ void topk_tail(const LogitsArgs& a, unsigned int* err
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) *a.counter = 0u;
+  if (threadIdx.x == 0) *a.counter = 0u;       // ready for the next call
+  if (threadIdx.x < m) tau[threadIdx.x] = 0u;
+}
+
+// The offset sum of one 16-byte piece of 8 activations: off * sum(x); with
+// kScaled, the halves at elements 2, 3, 6, 7 hold x/16 and weigh 1152, the
+// others weigh 1032 (Int4F16Scaled).
+template <typename XT, bool kScaled>
+__device__ __forceinline__ float corr_piece(const uint4& v, float off) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float a = 0.f, b = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float lo = scale_bits_to_f32<XT>((uint16_t)(w[q] & 0xFFFFu));
+    const float hi = scale_bits_to_f32<XT>((uint16_t)(w[q] >> 16));
+    if (kScaled && (q & 1)) b += lo + hi;
+    else a += lo + hi;
+  }
+  return kScaled ? 1032.0f * a + 1152.0f * b : off * a;
 }
 
 // tw:  packed weight, 16-row x 128-byte boxes (partial blocks)
@@ -201,6 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned int* flags = reinterpret_cast<unsigned int*>(empty + kStages);  // [0] bad, [1] last
   unsigned long long* red = reinterpret_cast<unsigned long long*>(sm + p.off_red);
   float* corr = reinterpret_cast<float*>(sm + p.off_corr);   // [kMaxTok][ngroups]
+  float* svals = reinterpret_cast<float*>(sm + p.off_vals);
+  int* blk_stage = reinterpret_cast<int*>(sm + p.off_blk);   // [kStages]
+  int* blk_list = blk_stage + kStages;                        // [cap_units]
+  const int U = p.unit_tiles;
 
   const LogitsArgs& a = p.a;
   const int lane = threadIdx.x & 31;
@@ -218,8 +387,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  const int T0 = (int)(((long long)p.tiles_total * blockIdx.x) / gridDim.x);
-  const int T1 = (int)(((long long)p.tiles_total * (blockIdx.x + 1)) / gridDim.x);
   bool bad = false;
 
   if (warp == kConsumers) {
@@ -233,14 +400,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t ephase = 0;
       int j = 0, issued = 0;
-      for (int tb = T0, blk = 0; tb < T1; tb += kBlockTiles, ++blk) {
-        const int ntb = min(kBlockTiles, T1 - tb);
+      // Work units: the CTA's first is its own index; later ones come from
+      // the shared counter (CTAs that stream faster take more) or, without
+      // one, in a fixed stride.  The next id is taken when a unit starts, so
+      // the atomic's latency hides behind that unit's copies; an id is only
+      // taken when the CTA has room to process it.
+      int b = (int)blockIdx.x;
+      for (int lb = 0; !bad && b < p.units_total && lb < p.cap_units; ++lb) {
+        int nextb = p.units_total;
+        if (lb + 1 < p.cap_units)
+          nextb = p.sched ? (int)atomicAdd(p.sched, 1u) + (int)gridDim.x : b + (int)gridDim.x;
+        blk_list[lb] = b;
+        const int tb = b * U;
+        const int ntb = min(U, p.tiles_total - tb);
         const bool sc_bulk = p.scales_aligned && (tb + ntb) * 16 <= n;
         const uint32_t sbytes = (uint32_t)(ntb * 16 * p.ngroups * 2);
         for (int c = 0; c < p.chunks; ++c, ++j) {
           // stage reuse: wait until all consumers released its previous fill
           if (j >= kStages && !bad) bad = !mbar_wait(&empty[stage], ephase ^ 1u);
           if (!bad) {
+            blk_stage[stage] = b;
             uint32_t bytes = (uint32_t)(ntb * kTileBytes);
             if (!XRES) bytes += (uint32_t)(kUnits * m * 128);
             if (c == 0 && sc_bulk) bytes += sbytes;
@@ -259,12 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(xdst + u * p.xbox_bytes, &tx, c * KC + u * 64, 0, &full[stage]);
             }
             if (c == 0 && sc_bulk)
-              bulk_load(sm + p.off_s + (blk % p.nsb) * p.sbuf_bytes,
+              bulk_load(sm + p.off_s + (lb % p.nsb) * p.sbuf_bytes,
                         scales + (size_t)tb * 16 * p.ngroups * 2, sbytes, &full[stage]);
             issued = j + 1;
           }
           if (++stage == kStages) { stage = 0; ephase ^= 1u; }
         }
+        b = nextb;
       }
       // Every copy this CTA issued must have landed before it can finish: the
       // latest fill of slot s completes phase (fills_of_s - 1) & 1.  On the
@@ -272,6 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages && s < issued; ++s) {
         const int fills = (issued - 1 - s) / kStages + 1;
         if (!mbar_wait(&full[s], (uint32_t)((fills - 1) & 1))) bad = true;
+      }
+      // End of work: one more stage, unit id -1, completed by a plain arrive
+      // (after the copies above, so no copy phase is pending on its slot).
+      if (!bad) {
+        if (j >= kStages) bad = !mbar_wait(&empty[stage], ephase ^ 1u);
+        if (!bad) {
+          blk_stage[stage] = -1;
+          mbar_arrive(&full[stage]);
+        }
       }
     }
   } else {
@@ -295,25 +484,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   ((piece ^ (tok & 7)) * 16)) = v;
       }
     }
-    // (2) per (token, group): the offset the MMA sums picked up
+    // (2) per (token, group): the offset the MMA sums picked up, summed from
+    //     16-byte pieces (the resident copy when there is one, as the MMA
+    //     sees it); absent tokens get 0
     if constexpr (CF::kCorr) {
+      if (XRES) consumer_sync();
       const int G = p.gunits * 64;
-      for (int pr = warp; pr < kMaxTok * p.ngroups; pr += kConsumers) {
+      for (int i = m * p.ngroups + threadIdx.x; i < kMaxTok * p.ngroups; i += kConsumers * 32)
+        corr[i] = 0.f;
+      for (int pr = warp; pr < m * p.ngroups; pr += kConsumers) {
         const int tok = pr / p.ngroups, gidx = pr - tok * p.ngroups;
         float s = 0.f;
-        if (tok < m) {
-          for (int e = lane; e < G; e += 32) {
-            const XT xv = xg[(size_t)tok * k + gidx * G + e];
-            if constexpr (CF::kScaledX) {
-              const int j = e & 7;
-              if (j == 2 || j == 3 || j == 6 || j == 7)
-                s += 1152.0f * to_f32(__hmul(xv, __float2half_rn(0.0625f)));
-              else
-                s += 1032.0f * to_f32(xv);
-            } else {
-              s += Codes::kOffset * to_f32(xv);
-            }
+        for (int e = lane * 8; e < G; e += 256) {
+          const int kk = gidx * G + e;
+          uint4 v;
+          if (XRES) {
+            const int U = kk >> 6, piece = (kk >> 3) & 7;
+            v = *reinterpret_cast<const uint4*>(sm + p.off_x + (U * m + tok) * 128 +
+                                                ((piece ^ (tok & 7)) * 16));
+          } else {
+            v = *reinterpret_cast<const uint4*>(xg + (size_t)tok * k + kk);
           }
+          s += corr_piece<XT, CF::kScaledX>(v, Codes::kOffset);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
@@ -348,13 +540,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int stage = 0;
     uint32_t fphase = 0;
-    for (int tb = T0, blk = 0; tb < T1; tb += kBlockTiles, ++blk) {
-      const int ntb = min(kBlockTiles, T1 - tb);
+    int lb = 0;
+    for (;; ++lb) {
+      // the stage of a unit's first chunk names the unit (-1: no more work)
+      if (!bad) bad = !mbar_wait(&full[stage], fphase);
+      if (bad) break;
+      const int ub = blk_stage[stage];
+      if (ub < 0) break;
+      const int tb = ub * U;
+      const int ntb = min(U, p.tiles_total - tb);
       const bool active = warp < ntb;
       const bool sc_bulk = p.scales_aligned && (tb + ntb) * 16 <= n;
       const int row_a = (tb + warp) * 16 + g, row_b = row_a + 8;
       const uint16_t* sbuf = reinterpret_cast<const uint16_t*>(sm + p.off_s +
-                                                               (blk % p.nsb) * p.sbuf_bytes);
+                                                               (lb % p.nsb) * p.sbuf_bytes);
       float acc[NT][4], part[NT][4];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -373,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int u_in_group = 0, gi = 0;
 
       for (int c = 0; c < p.chunks; ++c) {
-        if (!bad) bad = !mbar_wait(&full[stage], fphase);
+        if (c > 0 && !bad) bad = !mbar_wait(&full[stage], fphase);
         if (active && !bad) {
           const uint32_t wst = base + stage * kStageWBytes + warp * kTileBytes;
           const uint32_t xst = XRES ? base + p.off_x + (uint32_t)(c * kUnits) * xunit_stride
@@ -483,25 +682,43 @@ __global__ void __launch_bounds__(kThreads, 1)
               float v = acc[nt][c];
               if (a.bias) v += to_f32(reinterpret_cast<const XT*>(a.bias)[row]);
               reinterpret_cast<XT*>(a.logits)[(size_t)tok * n + row] = from_f32<XT>(v);
-              if (a.topk > 0) a.scratch[(size_t)tok * n + row] = v;
+              if (a.topk > 0) {
+                if (p.vals_stride > 0)
+                  svals[tok * p.vals_stride + lb * U * 16 + (row - tb * 16)] = v;
+                else
+                  a.scratch[(size_t)tok * n + row] = v;
+              }
             }
           }
       }
+      if (bad) break;
     }
+    if (threadIdx.x == 0) flags[2] = (unsigned int)lb;   // units this CTA processed
   }
 
   if (bad) atomicOr(&flags[0], 1u);
   __syncthreads();
   const bool cta_bad = flags[0] != 0u;
   if (cta_bad && threadIdx.x == 0 && p.err) atomicOr(p.err, 1u);
+  // Every producer of the grid is done taking units once all CTAs got here:
+  // the last CTA to arrive resets the unit counter for the next launch.
+  if (p.sched && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      p.sched[0] = 0u;
+      p.sched[1] = 0u;
+    }
+  }
   if (a.topk <= 0) return;
 
   // ---------------- top-K: per-CTA selection, last-CTA merge ----------------
-  const int row_begin = T0 * 16, row_end = min(T1 * 16, n);
+  SelWork& W = *reinterpret_cast<SelWork*>(sm);
+  const float* sv = p.vals_stride > 0 ? svals : nullptr;
+  const int nunits = (int)flags[2];
   if (a.topk <= 8)
-    topk_tail<8, XT>(a, p.err, red, flags, row_begin, row_end, cta_bad);
+    topk_tail<8, XT>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
   else
-    topk_tail<16, XT>(a, p.err, red, flags, row_begin, row_end, cta_bad);
+    topk_tail<16, XT>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
 }
 
 template <int BITS, typename XT, typename ST, int NT, bool XRES>

@@ -229,8 +229,9 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   base.k = (int)k;
   base.bias = bias;
   base.topk = topk;
+  // the counter block also schedules the decode kernel's work units
+  if (ws) base.counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
   if (topk > 0) {
-    base.counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
     base.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
     base.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
     base.tickets = reinterpret_cast<unsigned int*>(ws + lay.tickets_off);

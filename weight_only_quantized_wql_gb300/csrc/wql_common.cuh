@@ -229,6 +229,7 @@ template <> struct OffsetCodes<8, __nv_bfloat16> {   // exact q (no offset)
 // the per-group offset is 1032*sum(x) over the other elements plus
 // 1152*sum(x') over these.
 struct Int4F16Scaled {
+  static constexpr float kOffset = 1032.0f;   // of elements 0, 1, 4, 5
   static __device__ __forceinline__ void run(uint32_t w, uint32_t (&out)[4]) {
     const uint32_t m = 0x64006400u;
     const uint32_t hi = w >> 8;
