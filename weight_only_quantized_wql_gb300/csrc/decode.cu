@@ -79,9 +79,8 @@ Layout choose(int m, int k, int bits, int group_eff, int cap_units, int vals_row
   return L;
 }
 
-// Work split.  A unit is up to kBlockTiles 16-row tiles (one TMA box per
-// chunk when full); smaller units when there are too few for about three per
-// CTA.  CTAs take units from a counter in the workspace, so those whose
+// Work split.  A unit is kBlockTiles 16-row tiles (one TMA box per chunk
+// when full), halved while there are too few for about three per CTA.  CTAs take units from a counter in the workspace, so those whose
 // copies stream faster take more; cap_units bounds one CTA's share (room for
 // its unit list and top-K rows) and is never below an even share.
 struct Split {
@@ -93,9 +92,9 @@ Split split_work(int tiles_total, bool dynamic) {
   int ctas = device_sm_count();
   if (ctas > WQL_MAX_CTAS) ctas = WQL_MAX_CTAS;
   if (ctas < 1) ctas = 1;
+  // a power of two, so that a row's place in a CTA's list is a shift and mask
   int u = kBlockTiles;
-  if (tiles_total < 3 * kBlockTiles * ctas) u = (tiles_total + 3 * ctas - 1) / (3 * ctas);
-  if (u < 1) u = 1;
+  while (u > 1 && tiles_total < 3 * u * ctas) u >>= 1;
   w.unit_tiles = u;
   w.units_total = (tiles_total + u - 1) / u;
   w.ctas = ctas < w.units_total ? ctas : w.units_total;
@@ -139,6 +138,8 @@ cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s
   p.err = err;
   p.tiles_total = tiles_total;
   p.unit_tiles = w.unit_tiles;
+  p.unit_rows_log2 = 4;
+  while ((16 << (p.unit_rows_log2 - 4)) < w.unit_tiles * 16) ++p.unit_rows_log2;
   p.units_total = w.units_total;
   p.cap_units = w.cap_units;
   p.sched = dynamic ? a.counter + 2 : nullptr;

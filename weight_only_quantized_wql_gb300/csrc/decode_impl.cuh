@@ -62,7 +62,8 @@ constexpr int kTauWord = 16;                     // workspace word of token 0's 
 struct DecodeParams {
   LogitsArgs a;
   int tiles_total;      // ceil(n / 16)
-  int unit_tiles;       // 16-row tiles per work unit (<= kBlockTiles)
+  int unit_tiles;       // 16-row tiles per work unit (a power of two <= kBlockTiles)
+  int unit_rows_log2;   // log2(16 * unit_tiles)
   int units_total;      // ceil(tiles_total / unit_tiles)
   int cap_units;        // most units one CTA takes (cap_units * grid >= units_total)
   unsigned int* sched;  // [0] next unit - grid, [1] CTAs done; null: static units
@@ -88,6 +89,9 @@ struct SelWork {
   unsigned long long cand[kMaxTok][kSelCap];   // the kept keys
 };
 static_assert(sizeof(SelWork) <= (size_t)kStages * kStageWBytes, "selection area > ring");
+// the rest of the ring stages the CTAs' candidates for the final merge
+constexpr size_t kStageKeyOff = (sizeof(SelWork) + 127) / 128 * 128;
+constexpr size_t kStageKeyBytes = (size_t)kStages * kStageWBytes - kStageKeyOff;
 
 __host__ __device__ constexpr uint32_t round_up_u32(uint32_t v, uint32_t a) {
   return (v + a - 1) / a * a;
@@ -139,74 +143,139 @@ __device__ __forceinline__ void select_topk(int m, int K, int count, unsigned lo
   }
 }
 
-// The K-th largest of the 32 lanes' values (0 if fewer than K are non-zero):
-// K rounds of a warp maximum, each removing one lane that holds it.
-template <int KT>
-__device__ __forceinline__ uint32_t warp_kth_u32(uint32_t v, int K) {
+// Order-preserving 32-bit key of a value (the high half of topk_key): NaN 0.
+__device__ __forceinline__ uint32_t value_key(float v) {
+  if (v != v) return 0u;
+  const uint32_t b = __float_as_uint(v + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// The K-th largest of the 32 lanes' values (K <= 32), on every lane: each
+// lane ranks its value against all others (ties by lane), 32 independent
+// shuffles, and the lane of rank K-1 broadcasts it.
+__device__ __forceinline__ uint32_t warp_kth_rank(uint32_t v, int K) {
   const int lane = threadIdx.x & 31;
-  uint32_t kth = 0u;
+  int rank = 0;
 #pragma unroll
-  for (int r = 0; r < KT; ++r) {
-    if (r < K) {
-      const uint32_t mm = redux_max_u32(v);
-      kth = mm;
-      const unsigned int tied = __ballot_sync(0xFFFFFFFFu, v == mm);
-      if (lane == __ffs(tied) - 1) v = 0u;
-    }
+  for (int j0 = 0; j0 < 32; j0 += 8) {
+    uint32_t o[8];   // eight shuffles in flight before any is used
+#pragma unroll
+    for (int b = 0; b < 8; ++b) o[b] = __shfl_sync(0xFFFFFFFFu, v, j0 + b);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) rank += (o[b] > v || (o[b] == v && j0 + b < lane)) ? 1 : 0;
   }
-  return kth;
+  const unsigned int sel = __ballot_sync(0xFFFFFFFFu, rank == K - 1);
+  return __shfl_sync(0xFFFFFFFFu, v, __ffs(sel) - 1);
+}
+
+// Output of a warp's selection, per lane: the key for slot `slot` of the
+// descending top-K list (slot -1: this lane writes nothing).  Every slot
+// 0..K-1 is written by exactly one lane; kEmptyKey where there are fewer
+// than K entries.
+struct LaneSlot {
+  unsigned long long key;
+  int slot;
+};
+
+// Top K of c <= 32 unique keys held one per lane (lanes >= c: kEmptyKey):
+// each lane ranks its key by 32 shuffles and keeps slot = rank if rank < K.
+__device__ __forceinline__ LaneSlot warp_rank_of_32(unsigned long long key, int c, int K) {
+  const int lane = threadIdx.x & 31;
+  int rank = 0;
+#pragma unroll
+  for (int j0 = 0; j0 < 32; j0 += 8) {
+    unsigned long long o[8];   // eight shuffles in flight before any is used
+#pragma unroll
+    for (int b = 0; b < 8; ++b) o[b] = __shfl_sync(0xFFFFFFFFu, key, j0 + b);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) rank += o[b] > key ? 1 : 0;
+  }
+  LaneSlot r{kEmptyKey, -1};
+  if (lane < c) {
+    if (rank < K) r = {key, rank};
+  } else if (lane < K) {
+    r = {kEmptyKey, lane};   // fewer than K entries: the empty tail slots
+  }
+  return r;
+}
+
+// The same output from a descending list held identically by every lane.
+template <int KT>
+__device__ __forceinline__ LaneSlot lane_slot_of_list(const unsigned long long (&out)[KT], int K) {
+  const int lane = threadIdx.x & 31;
+  return lane < K ? LaneSlot{pick(out, lane), lane} : LaneSlot{kEmptyKey, -1};
 }
 
 // Threshold selection of the top-K keys of entries [0, count) per token, by
-// all threads of the CTA.  W.thr[t] must hold a lower bound of token t's K-th
+// all threads of the CTA.  vkey(t, i) reads entry i's value key (a 32-bit
+// key that orders values; 0 for NaN), fkey(t, i) its full 64-bit key (value
+// key high, index low).  W.thr[t] must hold a lower bound of token t's K-th
 // largest value key (0 if none) and W.cnt[t] zero, visible to all threads.
-// With kScan the CTA first raises each bound to the K-th largest of every
-// warp's lane maxima: K lanes hold disjoint entries at or above it, so it
-// does not exceed the token's K-th largest value.  The entries whose value
-// key reaches the bound are kept (all of the top K are among them) and warp
-// w < m selects token w's top K from those (out_tok = w; others -1).
-// Returns false, with nothing selected, if a token kept more than kSelCap
-// entries (many equal values); the caller then selects exhaustively.
-template <int KT, bool kScan, typename Load>
-__device__ __forceinline__ bool cta_topk(int m, int K, int count, Load load, SelWork& W,
-                                         unsigned long long (&out)[KT], int& out_tok) {
+// Each token's entries are spread over up to kSelWarps warps; every warp
+// raises the bound to the K-th largest of its lanes' maxima (K lanes hold
+// disjoint entries at or above it, so it does not exceed the token's K-th
+// largest value).  The entries whose value key reaches the bound are kept
+// (all of the top K are among them) and warp w < m selects token w's top K
+// from those (out_tok = w, slots in `res`; others -1).  Returns false, with
+// nothing selected, if a token kept more than kSelCap entries (many equal
+// values); the caller then selects exhaustively.
+constexpr int kSelWarps = 4;
+template <int KT, typename VKey, typename FKey>
+__device__ __forceinline__ bool cta_topk(int m, int K, int count, VKey vkey, FKey fkey,
+                                         SelWork& W, LaneSlot& res, int& out_tok) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int slices = max(1, kWarpsAll / m);
+  const int slices = max(1, min(kSelWarps, kWarpsAll / m));
   const bool worker = warp < slices * m;
   const int tok = warp % m, sl = warp / m;
   const int step = slices * 32;
-  if (kScan) {
-    if (worker) {
-      uint32_t mx = 0u;
-      for (int i0 = sl * 32 + lane; i0 < count; i0 += 8 * step) {
-        unsigned long long v[8];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const int i = i0 + b * step;
-          v[b] = i < count ? load(tok, i) : kEmptyKey;
-        }
-#pragma unroll
-        for (int b = 0; b < 8; ++b) mx = max(mx, (uint32_t)(v[b] >> 32));
-      }
-      const uint32_t kth = warp_kth_u32<KT>(mx, K);
-      if (lane == 0 && kth > 0u) atomicMax(&W.thr[tok], kth);
-    }
-    __syncthreads();
-  }
   if (worker) {
-    const uint32_t th = W.thr[tok];
+    uint32_t mx = 0u;
     for (int i0 = sl * 32 + lane; i0 < count; i0 += 8 * step) {
-      unsigned long long v[8];
+      uint32_t v[8];
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
         const int i = i0 + b * step;
-        v[b] = i < count ? load(tok, i) : kEmptyKey;
+        v[b] = vkey(tok, min(i, count - 1));
+        if (i >= count) v[b] = 0u;
       }
 #pragma unroll
+      for (int b = 0; b < 8; ++b) mx = max(mx, v[b]);
+    }
+    const uint32_t kth = warp_kth_rank(mx, K);
+    if (lane == 0 && kth > 0u) atomicMax(&W.thr[tok], kth);
+  }
+  __syncthreads();
+  if (worker) {
+    const uint32_t th = W.thr[tok];
+    // warp-uniform trip count (the ballots below need every lane)
+    for (int w0 = sl * 32; w0 < count; w0 += 8 * step) {
+      const int i0 = w0 + lane;
+      uint32_t v[8];
+#pragma unroll
       for (int b = 0; b < 8; ++b) {
-        if (v[b] != kEmptyKey && (uint32_t)(v[b] >> 32) >= th) {
-          const unsigned int at = atomicAdd(&W.cnt[tok], 1u);
-          if (at < (unsigned int)kSelCap) W.cand[tok][at] = v[b];
+        const int i = i0 + b * step;
+        v[b] = vkey(tok, min(i, count - 1));
+      }
+      // one shared atomic per warp for the batch's passing entries
+      unsigned int mask[8];
+      int total = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        mask[b] = __ballot_sync(0xFFFFFFFFu, i0 + b * step < count && v[b] >= th);
+        total += __popc(mask[b]);
+      }
+      if (total > 0) {
+        unsigned int at = 0u;
+        if (lane == 0) at = atomicAdd(&W.cnt[tok], (unsigned int)total);
+        at = __shfl_sync(0xFFFFFFFFu, at, 0);
+        const unsigned int lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (mask[b] >> lane & 1u) {
+            const unsigned int pos = at + __popc(mask[b] & lt);
+            if (pos < (unsigned int)kSelCap) W.cand[tok][pos] = fkey(tok, i0 + b * step);
+          }
+          at += __popc(mask[b]);
         }
       }
     }
@@ -218,96 +287,146 @@ __device__ __forceinline__ bool cta_topk(int m, int K, int count, Load load, Sel
   if (overflow) return false;
   if (warp < m) {
     const int c = (int)W.cnt[warp];
-    unsigned long long list[KT];
+    if (c <= 32) {
+      res = warp_rank_of_32(lane < c ? W.cand[warp][lane] : kEmptyKey, c, K);
+    } else {
+      unsigned long long list[KT], out[KT];
 #pragma unroll
-    for (int i = 0; i < KT; ++i) list[i] = kEmptyKey;
-    for (int i = lane; i < c; i += 32) list_insert<KT>(list, W.cand[warp][i]);
-    warp_merge_topk_redux<KT>(list, K, out);
+      for (int i = 0; i < KT; ++i) list[i] = kEmptyKey;
+      for (int i = lane; i < c; i += 32) list_insert<KT>(list, W.cand[warp][i]);
+      warp_merge_topk_redux<KT>(list, K, out);
+      res = lane_slot_of_list<KT>(out, K);
+    }
     out_tok = warp;
   }
   return true;
 }
 
+// Ticket of the last-CTA merge: an atomic add whose release makes this CTA's
+// candidate writes (ordered before it by the preceding block barrier)
+// visible before the ticket, and whose acquire, for the last CTA, makes the
+// other CTAs' candidates visible after it.
+__device__ __forceinline__ unsigned int ticket_add(unsigned int* t) {
+  unsigned int old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+  return old;
+}
+
 // This CTA's candidates, the ticket, and (last CTA only) the final merge.
-// The CTA's rows are its nunits work units in the order it took them
-// (unit ids in blk_list); entry i is row blk_list[i / R] * R + i % R with R
-// the rows per unit.  svals: their fp32 logits in shared memory
-// ([token][vals_stride], entry order), or null for the global scratch row.
-template <int KT, typename XT>
-__device__ __forceinline__ void topk_tail(const DecodeParams& p, SelWork& W,
+// The CTA's rows are its nunits work units in the order it took them (unit
+// ids in blk_list, 2^rlog rows each; the grid's last unit, cut at n, is
+// always a CTA's last).  svals: their fp32 logits in shared memory
+// ([token][vals_stride], entry li * R + r), or null for the global scratch
+// row.
+template <int KT, typename XT, bool kSmemVals>
+__device__ __noinline__ void topk_tail(const DecodeParams& p, SelWork& W,
                                           unsigned long long* red, unsigned int* flags,
                                           int nunits, const int* blk_list, bool cta_bad,
-                                          const float* svals) {
+                                          const float* svals, unsigned long long* stage_keys) {
   const LogitsArgs& a = p.a;
   unsigned int* err = p.err;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int m = a.m, n = a.n, K = a.topk;
   unsigned int* tau = a.counter + kTauWord;   // per-token bound on the K-th value key
   if (!cta_bad) {
-    const int R = p.unit_tiles * 16;
-    const int count = nunits * R;
+    const int rlog = p.unit_rows_log2, R = 1 << rlog;
+    const int count = nunits > 0 ? (nunits - 1) * R + min(R, n - blk_list[nunits - 1] * R) : 0;
     const int vs = p.vals_stride;
-    auto load = [&](int tk, int i) -> unsigned long long {
-      const int li = i / R;
-      const int row = blk_list[li] * R + (i - li * R);
-      if (row >= n) return kEmptyKey;
-      const float v = svals ? svals[tk * vs + i] : __ldcg(a.scratch + (size_t)tk * n + row);
-      return topk_key(v, (uint32_t)row);
+    auto rowof = [&](int i) { return blk_list[i >> rlog] * R + (i & (R - 1)); };
+    auto value = [&](int tk, int i) -> float {
+      if constexpr (kSmemVals) return svals[tk * vs + i];
+      else return __ldcg(a.scratch + (size_t)tk * n + rowof(i));
     };
+    auto vkey = [&](int tk, int i) { return value_key(value(tk, i)); };
+    auto key = [&](int tk, int i) { return topk_key(value(tk, i), (uint32_t)rowof(i)); };
     if (threadIdx.x < m) {
       W.thr[threadIdx.x] = 0u;
       W.cnt[threadIdx.x] = 0u;
     }
     __syncthreads();
-    unsigned long long best[KT];
+    LaneSlot res{kEmptyKey, -1};
     int tok;
-    if (!cta_topk<KT, true>(m, K, count, load, W, best, tok))
-      select_topk<KT>(m, K, count, red, load, best, tok);
-    if (tok >= 0) {
-      const unsigned long long mine = pick(best, lane);
-      if (lane < K) a.cand[((size_t)tok * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
-      const unsigned long long kth = pick(best, K - 1);
-      if (lane == 0 && kth != kEmptyKey) atomicMax(tau + tok, (uint32_t)(kth >> 32));
-      __threadfence();
+    if (!cta_topk<KT>(m, K, count, vkey, key, W, res, tok)) {
+      unsigned long long best[KT];
+      select_topk<KT>(m, K, count, red, key, best, tok);
+      res = lane_slot_of_list<KT>(best, K);
+    }
+    if (tok >= 0 && res.slot >= 0) {
+      a.cand[((size_t)tok * WQL_MAX_CTAS + blockIdx.x) * K + res.slot] = res.key;
+      // every CTA's K-th value bounds the final K-th value from below
+      if (res.slot == K - 1 && res.key != kEmptyKey)
+        atomicMax(tau + tok, (uint32_t)(res.key >> 32));
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned int ticket = atomicAdd(a.counter, 1u);
-    flags[1] = (ticket == gridDim.x - 1) ? 1u : 0u;
-  }
+  if (threadIdx.x == 0) flags[1] = (ticket_add(a.counter) == gridDim.x - 1) ? 1u : 0u;
   __syncthreads();
   if (flags[1] == 0u) return;
-  __threadfence();
-  const bool any_bad = (__ldcg(err) != 0u);
-  unsigned long long best[KT];
-  int tok = -1;
-  if (!any_bad) {
-    // every CTA's K-th value bounds the final K-th value from below
+  // The error word (set by any CTA whose bounded wait timed out, before its
+  // ticket): its load is in flight during the staging; with an error the
+  // results are replaced by "no entries" at the end.  A CTA that timed out
+  // itself skips the staging (copies of its own may still land in the ring).
+  const unsigned int errv = __ldcg(err);
+  if (!cta_bad) {
+    // the CTAs' candidates, staged in shared memory a group of tokens at a time
     const int count = (int)gridDim.x * K;
-    auto load = [&](int tk, int i) { return __ldcg(a.cand + (size_t)tk * WQL_MAX_CTAS * K + i); };
-    if (threadIdx.x < m) {
-      W.thr[threadIdx.x] = __ldcg(tau + threadIdx.x);
-      W.cnt[threadIdx.x] = 0u;
-    }
-    __syncthreads();
-    if (!cta_topk<KT, false>(m, K, count, load, W, best, tok))
-      select_topk<KT>(m, K, count, red, load, best, tok);
-  } else if (warp < m) {
-    tok = warp;   // an internal wait timed out somewhere: report no entries
+    const int group = max(1, min(m, (int)(kStageKeyBytes / ((size_t)count * 8))));
+    for (int t0 = 0; t0 < m; t0 += group) {
+      const int mg = min(group, m - t0);
+      // eight loads in flight per thread
+      const int total = mg * count;
+      if (mg == 1) {
+        const unsigned long long* src = a.cand + (size_t)t0 * WQL_MAX_CTAS * K;
+        for (int i0 = threadIdx.x; i0 < count; i0 += 8 * (int)blockDim.x) {
+          unsigned long long v[8];
 #pragma unroll
-    for (int i = 0; i < KT; ++i) best[i] = kEmptyKey;
-  }
-  if (tok >= 0) {
-    const unsigned long long mine = pick(best, lane);
-    if (lane < K) {
-      const bool ok = !any_bad && mine != kEmptyKey;
-      a.topk_idx[(size_t)tok * K + lane] = ok ? key_index(mine) : -1;
-      a.topk_val[(size_t)tok * K + lane] = ok ? key_value(mine) : __int_as_float(0x7FC00000);
+          for (int b = 0; b < 8; ++b) v[b] = __ldcg(src + min(i0 + b * (int)blockDim.x, count - 1));
+#pragma unroll
+          for (int b = 0; b < 8; ++b)
+            if (i0 + b * (int)blockDim.x < count) stage_keys[i0 + b * (int)blockDim.x] = v[b];
+        }
+      } else
+      for (int i0 = threadIdx.x; i0 < total; i0 += 8 * (int)blockDim.x) {
+        unsigned long long v[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const int i = min(i0 + b * (int)blockDim.x, total - 1);
+          const int tl = i / count;
+          v[b] = __ldcg(a.cand + (size_t)(t0 + tl) * WQL_MAX_CTAS * K + (i - tl * count));
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+          if (i0 + b * (int)blockDim.x < total) stage_keys[i0 + b * (int)blockDim.x] = v[b];
+      }
+      if (threadIdx.x < mg) {
+        W.thr[threadIdx.x] = __ldcg(tau + t0 + threadIdx.x);
+        W.cnt[threadIdx.x] = 0u;
+      }
+      __syncthreads();
+      auto key = [&](int tl, int i) { return stage_keys[tl * count + i]; };
+      auto vkey = [&](int tl, int i) { return (uint32_t)(stage_keys[tl * count + i] >> 32); };
+      LaneSlot res{kEmptyKey, -1};
+      int tok;
+      if (!cta_topk<KT>(mg, K, count, vkey, key, W, res, tok)) {
+        unsigned long long best[KT];
+        select_topk<KT>(mg, K, count, red, key, best, tok);
+        res = lane_slot_of_list<KT>(best, K);
+      }
+      if (tok >= 0 && res.slot >= 0) {
+        const bool ok = errv == 0u && res.key != kEmptyKey;
+        const size_t o = (size_t)(t0 + tok) * K + res.slot;
+        a.topk_idx[o] = ok ? key_index(res.key) : -1;
+        a.topk_val[o] = ok ? key_value(res.key) : __int_as_float(0x7FC00000);
+      }
+      __syncthreads();
+    }
+  } else {
+    // this CTA timed out: report no entries
+    for (int i = threadIdx.x; i < m * K; i += blockDim.x) {
+      a.topk_idx[i] = -1;
+      a.topk_val[i] = __int_as_float(0x7FC00000);
     }
   }
-  __syncthreads();
   if (threadIdx.x == 0) *a.counter = 0u;       // ready for the next call
   if (threadIdx.x < m) tau[threadIdx.x] = 0u;
 }
@@ -352,7 +471,7 @@ struct CodesFor<4, __half, true> {
 template <int BITS, typename XT, typename ST, int NT, bool XRES>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap twb,
-                  const __grid_constant__ CUtensorMap tx, const DecodeParams p) {
+                  const __grid_constant__ CUtensorMap tx, const __grid_constant__ DecodeParams p) {
   using CF = CodesFor<BITS, XT, XRES>;
   using Codes = typename CF::type;
   constexpr int kUnits = BITS == 4 ? 4 : 2;        // 64-column units per chunk
@@ -452,6 +571,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages && s < issued; ++s) {
         const int fills = (issued - 1 - s) / kStages + 1;
         if (!mbar_wait(&full[s], (uint32_t)((fills - 1) & 1))) bad = true;
+      }
+      // This producer takes no more units (its last take has returned): the
+      // last producer of the grid to get here resets the counter for the
+      // next launch.
+      if (p.sched && atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+        p.sched[0] = 0u;
+        p.sched[1] = 0u;
       }
       // End of work: one more stage, unit id -1, completed by a plain arrive
       // (after the copies above, so no copy phase is pending on its slot).
@@ -700,25 +826,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const bool cta_bad = flags[0] != 0u;
   if (cta_bad && threadIdx.x == 0 && p.err) atomicOr(p.err, 1u);
-  // Every producer of the grid is done taking units once all CTAs got here:
-  // the last CTA to arrive resets the unit counter for the next launch.
-  if (p.sched && threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
-      p.sched[0] = 0u;
-      p.sched[1] = 0u;
-    }
-  }
   if (a.topk <= 0) return;
 
   // ---------------- top-K: per-CTA selection, last-CTA merge ----------------
   SelWork& W = *reinterpret_cast<SelWork*>(sm);
   const float* sv = p.vals_stride > 0 ? svals : nullptr;
   const int nunits = (int)flags[2];
-  if (a.topk <= 8)
-    topk_tail<8, XT>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
-  else
-    topk_tail<16, XT>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
+  unsigned long long* stage_keys = reinterpret_cast<unsigned long long*>(sm + kStageKeyOff);
+  if (sv) {
+    if (a.topk <= 8)
+      topk_tail<8, XT, true>(p, W, red, flags, nunits, blk_list, cta_bad, sv, stage_keys);
+    else
+      topk_tail<16, XT, true>(p, W, red, flags, nunits, blk_list, cta_bad, sv, stage_keys);
+  } else {
+    if (a.topk <= 8)
+      topk_tail<8, XT, false>(p, W, red, flags, nunits, blk_list, cta_bad, sv, stage_keys);
+    else
+      topk_tail<16, XT, false>(p, W, red, flags, nunits, blk_list, cta_bad, sv, stage_keys);
+  }
 }
 
 template <int BITS, typename XT, typename ST, int NT, bool XRES>
