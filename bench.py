@@ -6,12 +6,16 @@ for each M in (1, 32, 256), wql_logits with top-8 candidates followed by
 wql_topk_rescore of those candidates from the fp16 reference rows.
 Quantisation (load time) is timed once, outside the steps.
 
-Timing: CUDA events on the launching stream around every call; the calls
-run back to back, and every call reads one of four copies of the quantised
-weight in turn, so the copy it reads was not touched by the three calls
-before it (3 x 83 MB > the 129 MB L2): weights always come from HBM.  `value`
-is the algorithmic bytes of the step (packed weight + scales + X + logits
-written + top-K + rescored rows) over the summed device time.  `--gpus N`
+Timing: each step is a CUDA-graph replay of its calls (captured once per
+phase of the copy rotation), bracketed by CUDA events on the launching
+stream, so the host's per-call launch work is not on the device timeline.
+Every call reads one of four copies of the quantised weight in turn, so the
+copy it reads was not touched by the three calls before it (3 x 83 MB > the
+129 MB L2): weights always come from HBM.  `value` is the algorithmic bytes
+of the step (packed weight + scales + X + logits written + top-K + rescored
+rows) over the summed device time.  `e2e` runs the same step as eager calls
+of the public API with X copied in from pinned host memory and the outputs
+copied back every step.  `--gpus N`
 under torchrun runs N independent replicas (the head is replicated, not
 sharded) and reports the units of all ranks over the slowest rank's time.
 
@@ -23,6 +27,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import math
 import json
 import os
 import statistics
@@ -201,46 +206,100 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     def rescore(m):
         wql.wql_topk_rescore(xs[m], w_ref, idx[m], val[m], outs[m])
 
-    def one_step(record):
-        per = {}
+    def one_step():
         for m in MS:
-            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-            a.record(stream)
             call(m)
-            b.record(stream)
             rescore(m)
-            c.record(stream)
-            per[m] = (a, b, c)
-        return per
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
+    # Warm-up, eager: sizes the workspace and loads every kernel before capture.
     for _ in range(args.warmup):
-        one_step(False)
+        one_step()
     torch.cuda.synchronize()
+
+    # The device-timed step is a CUDA graph replay: one graph per phase of the
+    # weight-copy rotation, so replay s reads exactly the copies an eager step
+    # s would.  The host's per-call launch work (ctypes marshalling, tensor-map
+    # encoding) then stays off the device timeline; the e2e leg below keeps it.
+    cap = torch.cuda.Stream(dev)
+    nph = N_COPIES // math.gcd(N_COPIES, len(MS))     # steps until the rotation repeats
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                fn()
+        stream.wait_stream(cap)
+        return g
+
+    graphs = []
+    n0 = wql.wql_launch_count()
+    for ph in range(nph):
+        counter[0] = ph * len(MS)
+        graphs.append(capture(one_step))
+    launches_per_step = (wql.wql_launch_count() - n0) // nph
+    for i in range(max(args.warmup, nph)):
+        graphs[i % nph].replay()
+    torch.cuda.synchronize()
+
     clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local_rank)
     barrier()
     torch.cuda.synchronize()
     clocks.start()
-    launches0 = wql.wql_launch_count()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     t_wall0 = time.perf_counter()
-    recs = [one_step(True) for _ in range(args.steps)]
+    for st in range(args.steps):
+        evs[st][0].record(stream)
+        graphs[st % nph].replay()
+        evs[st][1].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
-    launches = wql.wql_launch_count() - launches0
+    launches = launches_per_step * args.steps
     barrier()
     clk = clocks.stop()
-
-    logit_us = {m: [] for m in MS}
-    resc_us = {m: [] for m in MS}
-    for per in recs:
-        for m, (a, b, c) in per.items():
-            logit_us[m].append(a.elapsed_time(b) * 1e3)
-            resc_us[m].append(b.elapsed_time(c) * 1e3)
-    step_us = [sum(logit_us[m][i] + resc_us[m][i] for m in MS) for i in range(args.steps)]
+    step_us = [a.elapsed_time(b) * 1e3 for a, b in evs]
     dev_s = sum(step_us) * 1e-6
+
+    # ---- per-call breakdown: graphs of R calls of one kind, rotating copies ----
+    R = 20
+
+    def time_graph(g, reps=3):
+        g.replay()
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            per.append(a.elapsed_time(b) * 1e3 / R)
+        return sorted(per)
+
+    def logits_calls(m, topk):
+        def fn():
+            for r in range(R):
+                if topk:
+                    wql.wql_logits(xs[m], copies[r % N_COPIES], topk=topk, workspace=ws,
+                                   out=outs[m], topk_idx=idx[m], topk_val=val[m])
+                else:
+                    wql.wql_logits(xs[m], copies[r % N_COPIES], topk=0, workspace=ws,
+                                   out=outs[m])
+        return fn
+
+    def rescore_calls(m):
+        def fn():
+            for _ in range(R):
+                rescore(m)
+        return fn
+
+    logit_us = {m: time_graph(capture(logits_calls(m, TOPK))) for m in MS}
+    resc_us = {m: time_graph(capture(rescore_calls(m))) for m in MS}
 
     # ---- end to end: pinned host X in, logits + top-K out, every call ----
     hx = {m: xs[m].cpu().pin_memory() for m in MS}
@@ -272,24 +331,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     assert ws.error_word() == 0, "a kernel's bounded wait timed out"
 
     # ---- the dominant kernel alone: the logits call with the largest share
-    # of device time, repeated with top-K off, which is one launch of its
-    # logits kernel (decode_kernel for M <= 16, tc_logits_kernel above) ----
-    dom_m = max(MS, key=lambda m: sum(logit_us[m]))
-    kern_us = []
+    # of device time, with top-K off, which is one launch of its logits kernel
+    # per call (decode_kernel for M <= 16, tc_logits_kernel above) ----
+    dom_m = max(MS, key=lambda m: statistics.median(logit_us[m]))
     n0 = wql.wql_launch_count()
-    for it in range(args.warmup + max(args.steps, 10)):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c = copies[counter[0] % N_COPIES]
-        counter[0] += 1
-        a.record(stream)
-        wql.wql_logits(xs[dom_m], c, topk=0, workspace=ws, out=outs[dom_m])
-        b.record(stream)
-        if it >= args.warmup:
-            kern_us.append((a, b))
-    torch.cuda.synchronize()
-    kern_launches = wql.wql_launch_count() - n0
-    assert kern_launches == args.warmup + max(args.steps, 10), "one launch per call expected"
-    kern_us = [a.elapsed_time(b) * 1e3 for a, b in kern_us]
+    g_dom = capture(logits_calls(dom_m, 0))
+    assert wql.wql_launch_count() - n0 == R, "one launch per call expected"
+    kern_us = time_graph(g_dom, reps=max(3, args.steps // 4))
 
     # ---- reduce over ranks: max time ----
     vals = torch.tensor([dev_s, sum(e2e_us) * 1e-6, t_wall], dtype=torch.float64, device=dev)
@@ -302,7 +350,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     pk = peaks()
     total_bytes = step_bytes(MS) * args.steps * world
     value = total_bytes / dev_s / 1e9
-    med = {m: statistics.median(logit_us[m]) for m in MS}
+    med = {m: statistics.median(logit_us[m]) for m in MS}   # each entry: mean of R calls
     calls = {}
     for m in MS:
         b = logits_bytes(m, N_VOCAB, K_HIDDEN, 4, GROUP, topk=TOPK)
@@ -311,12 +359,12 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
         tfl = fl / (med[m] * 1e-6) / 1e12
         calls[f"M{m}"] = {
             "us_median": round(med[m], 2),
-            "us_p10": round(sorted(logit_us[m])[max(0, len(logit_us[m]) // 10)], 2),
+            "us_min": round(min(logit_us[m]), 2),
             "GBps": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
             "TFLOPs": round(tfl, 2), "frac_tensor": round(tfl / pk["bf16_tflops"], 4),
             "rescore_us": round(statistics.median(resc_us[m]), 2)}
     # dominant kernel, timed alone above (mean launch duration)
-    dom_us = statistics.mean(kern_us)
+    dom_us = statistics.median(kern_us)
     dom_flops = 2.0 * dom_m * N_VOCAB * K_HIDDEN
     dom_bytes = logits_bytes(dom_m, N_VOCAB, K_HIDDEN, 4, GROUP, topk=0)
     kern = "tc_logits_kernel" if dom_m > 16 else "decode_kernel"
@@ -346,7 +394,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
                    "ms": list(MS), "topk": TOPK, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {N_COPIES} rotating weight copies "
                          f"({N_COPIES * 83} MB), each call reads a copy untouched for 3 calls",
-                   "step_bytes": step_bytes(MS)},
+                   "step_bytes": step_bytes(MS),
+                   "timing": "device: CUDA-graph replay of each step (one graph per phase of "
+                             "the copy rotation), events around each replay; calls and "
+                             "roofline: graphs of 20 calls; e2e: eager public-API calls"},
         "calls": calls, "quantize_ms": round(quant_ms, 3),
         "roofline": roof,
         "cpu_baseline": None,

@@ -124,7 +124,15 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(device) -> ctypes.c_void_p:
+    """torch's current CUDA stream on `device` (the raw handle, read the
+    cheap way when this torch build offers it)."""
+    if _raw_stream is not None:
+        idx = device.index if device.index is not None else torch.cuda.current_device()
+        return ctypes.c_void_p(_raw_stream(idx))
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
@@ -143,8 +151,15 @@ class QuantizedWeight:
         return _DTYPE_CODE[self.scales.dtype]
 
     def _struct(self) -> _WqlWeight:
-        return _WqlWeight(self.bits, self.group, self.scale_dtype, 0, self.n, self.k,
-                          self.qweight.data_ptr(), self.scales.data_ptr())
+        # built once per (qweight, scales) storage; calls reuse it
+        key = (self.qweight.data_ptr(), self.scales.data_ptr(), self.bits, self.group,
+               self.n, self.k, self.scales.dtype)
+        cached = self.__dict__.get("_st")
+        if cached is None or cached[0] != key:
+            cached = (key, _WqlWeight(self.bits, self.group, self.scale_dtype, 0, self.n,
+                                      self.k, key[0], key[1]))
+            self.__dict__["_st"] = cached
+        return cached[1]
 
     def nbytes(self) -> int:
         return self.qweight.numel() * self.qweight.element_size() + \
@@ -186,8 +201,15 @@ def wql_launch_count() -> int:
     return int(load().wql_launch_count())
 
 
+_ws_sizes: dict = {}
+
+
 def wql_workspace_size(m: int, n: int, topk: int) -> int:
-    return int(load().wql_workspace_size(m, n, topk))
+    key = (m, n, topk)
+    v = _ws_sizes.get(key)
+    if v is None:
+        v = _ws_sizes[key] = int(load().wql_workspace_size(m, n, topk))
+    return v
 
 
 def wql_quantize(w: torch.Tensor, bits: int, group: int, scale_dtype=torch.float16,
