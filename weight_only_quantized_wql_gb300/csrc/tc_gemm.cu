@@ -12,16 +12,18 @@
 //    bytes per row (256 int4 / 128 int8 codes; 128-row 128B-swizzled boxes)
 //    and -- unless they stay resident for the whole launch -- the
 //    activations in 64-column boxes.
-//  * Warps 2..9 dequantise: thread pair (r, r+128) owns row r of the tile;
-//    per 64-column block each turns 32 codes into exact fp16 q (magic-number
-//    LOP3/PRMT), multiplies by the row's group scale (one fp16 rounding of
-//    q*s) and writes its half of the 128B-swizzled K-major A row the tensor
-//    core reads.
-//  * Warp 1 allocates tensor memory and one lane issues tcgen05.mma
-//    (kind::f16, 128 x N x 16) for every 16 columns, committing to
+//  * Warps 2..17 dequantise, as two groups of eight that fill A stages in
+//    turn; a stage holds two consecutive 64-column blocks (32 KB).  Within
+//    a group, thread pair (r, r+128) owns row r of the tile: per block it
+//    turns 32 codes into exact fp16 q (magic-number LOP3/PRMT), multiplies
+//    by the row's group scale (one fp16 rounding of q*s) and writes its
+//    half of the 128B-swizzled K-major A row the tensor core reads.
+//  * Warp 1 allocates tensor memory and runs the issue loop as a whole warp
+//    (warp-uniform indices and descriptors); one elected lane issues
+//    tcgen05.mma (kind::f16, 128 x N x 16), eight per A stage, committing to
 //    mbarriers that release the A / activation buffers and hand finished
 //    accumulators to the epilogue.
-//  * Warps 10..13 (one per TMEM lane quarter) read the accumulator with
+//  * Warps 18..21 (one per TMEM lane quarter) read the accumulator with
 //    tcgen05.ld, add the bias, round to fp16, transpose each 32 x 32 block
 //    through shared memory and store the logits with 16-byte stores.  Top-K
 //    candidates are chosen afterwards from these logits (topk_select.cu).
@@ -37,13 +39,19 @@ namespace wql {
 namespace {
 
 constexpr int kTileRows = 128;
-constexpr int kWarps = 14;
+constexpr int kWarps = 22;
 constexpr int kThreads = kWarps * 32;
-constexpr int kProducerWarp = 0, kMmaWarp = 1, kDequantWarp0 = 2, kEpilogueWarp0 = 10;
-constexpr int kDequantWarps = 8, kEpilogueWarps = 4;
+constexpr int kProducerWarp = 0, kMmaWarp = 1, kDequantWarp0 = 2, kEpilogueWarp0 = 18;
+constexpr int kDequantGroups = 2, kGroupWarps = 8;
+constexpr int kDequantWarps = kDequantGroups * kGroupWarps, kEpilogueWarps = 4;
 constexpr int kWChunkBytes = kTileRows * 128;     // one packed-weight chunk (16 KB)
 constexpr int kABytes = kTileRows * 128;          // one 64-column fp16 A block (16 KB)
-constexpr int kWStages = 3, kAStages = 3;
+constexpr int kStageBlocks = 2;                   // A blocks per stage: 8 MMAs per handshake
+constexpr int kAStageBytes = kStageBlocks * kABytes;
+constexpr int kMaxWStages = 8, kMinWStages = 3;   // packed-weight ring: as deep as smem allows
+constexpr int kMinAStages = 2, kMaxAStages = 3;   // A ring: 3 stages where smem allows
+static_assert(kStageBlocks == kDequantGroups, "each group fills one block of every stage");
+static_assert(kEpilogueWarp0 == kDequantWarp0 + kDequantWarps, "warp roles overlap");
 constexpr int kStageBytes = kEpilogueWarps * 32 * 32 * 2;   // logits staging, all warps
 
 struct TcParams {
@@ -56,6 +64,8 @@ struct TcParams {
   int x_resident;       // activations staged once per CTA
   int xstages;          // activation ring depth when not resident
   int acc_bufs;         // 1 or 2 accumulators in TMEM
+  int wstages;          // packed-weight ring depth (kMinWStages..kMaxWStages)
+  int astages;          // A ring depth (kMinAStages..kMaxAStages)
   uint32_t tmem_cols;   // power of two >= acc_bufs * npad
   uint32_t off_w, off_a, off_x, off_bar, off_s;
   uint32_t off_st;      // per-epilogue-warp logits staging (32 tokens x 32 rows fp16)
@@ -94,6 +104,17 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// One lane of the (fully active) warp: true there, false elsewhere.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xFFFFFFFF;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0u;
 }
 
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -160,10 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + p.off_bar);
   uint64_t* w_full = bars;
-  uint64_t* w_empty = w_full + kWStages;
-  uint64_t* a_full = w_empty + kWStages;
-  uint64_t* a_empty = a_full + kAStages;
-  uint64_t* x_full = a_empty + kAStages;
+  uint64_t* w_empty = w_full + kMaxWStages;
+  uint64_t* a_full = w_empty + kMaxWStages;
+  uint64_t* a_empty = a_full + kMaxAStages;
+  uint64_t* x_full = a_empty + kMaxAStages;
   uint64_t* x_empty = x_full + 4;
   uint64_t* acc_full = x_empty + 4;
   uint64_t* acc_empty = acc_full + 2;
@@ -181,12 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t xblock_bytes = (uint32_t)p.npad * 128u;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kWStages; ++s) {
+    for (int s = 0; s < p.wstages; ++s) {
       mbar_init(&w_full[s], 1);
       mbar_init(&w_empty[s], kDequantWarps);
     }
-    for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&a_full[s], kDequantWarps);
+    for (int s = 0; s < p.astages; ++s) {
+      mbar_init(&a_full[s], kDequantWarps);    // both groups, one block each
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < 4; ++s) {
@@ -240,19 +261,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++sfills;
         }
         for (int c = 0; c < p.chunks && !bad; ++c) {
-          if (wfills >= kWStages) bad = !mbar_wait(&w_empty[ws], wph ^ 1u);
+          if (wfills >= p.wstages) bad = !mbar_wait(&w_empty[ws], wph ^ 1u);
           if (bad) break;
           mbar_arrive_expect_tx(&w_full[ws], (uint32_t)kWChunkBytes);
           tma_load_2d(sm + p.off_w + ws * kWChunkBytes, &tw, c * 32, t * kTileRows, &w_full[ws]);
           ++wfills;
-          if (++ws == kWStages) { ws = 0; wph ^= 1u; }
+          if (++ws == p.wstages) { ws = 0; wph ^= 1u; }
         }
       }
       // every issued copy lands before the CTA can finish
       for (int s = 0; s < 2 && s < sfills; ++s)
         if (!mbar_wait(&s_full[s], (uint32_t)(((sfills - 1 - s) >> 1) & 1))) bad = true;
-      for (int s = 0; s < kWStages && s < wfills; ++s)
-        if (!mbar_wait(&w_full[s], (uint32_t)(((wfills - 1 - s) / kWStages) & 1))) bad = true;
+      for (int s = 0; s < p.wstages && s < wfills; ++s)
+        if (!mbar_wait(&w_full[s], (uint32_t)(((wfills - 1 - s) / p.wstages) & 1))) bad = true;
     } else if (lane == 1 && ntiles > 0) {
       prefetch_tmap(&tx);
       if (p.x_resident) {
@@ -280,62 +301,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer ------------------------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16(p.npad);
-      int as = 0, xs = 0, acc = 0;
-      uint32_t aph = 0, xph = 0, accph = 0;
-      int tiles_done = 0;
-      bool x_ready = false;
-      for (int t = T0; t < T1 && !bad; ++t, ++tiles_done) {
-        // wait for the epilogue to have drained this accumulator buffer
-        if (tiles_done >= p.acc_bufs) bad = !mbar_wait(&acc_empty[acc], accph ^ 1u);
-        if (bad) break;
+    // The whole warp runs the issue loop, so stage indices and operand
+    // descriptors are warp-uniform values; one elected lane issues the
+    // tcgen05 instructions (single-thread instructions) and their commits.
+    // One A-stage handshake covers kStageBlocks blocks (8 MMAs), which
+    // halves the waits per MMA: this one warp's loop sets the pace when the
+    // MMAs themselves are short.  The descriptors are built once and advanced
+    // by additions (the start-address field counts 16-byte units; every
+    // operand lies below 256 KB, so the field never carries).
+    const bool leader = elect_one();
+    const uint32_t idesc = idesc_f16(p.npad);
+    const uint64_t adesc0 = smem_desc_sw128(base + p.off_a);
+    const uint64_t xdesc0 = smem_desc_sw128(base + p.off_x);
+    const uint64_t xstep = (uint64_t)(xblock_bytes >> 4);
+    constexpr uint64_t kAStep = (uint64_t)(kABytes >> 4);
+    constexpr uint64_t kKStep = 32u >> 4;          // 16 fp16 columns of a K-major row
+    int as = 0, xs = 0, acc = 0;
+    uint32_t aph = 0, xph = 0, accph = 0;
+    int tiles_done = 0;
+    if (p.x_resident && T0 < T1) bad = !mbar_wait(&x_full[0], 0u);
+    for (int t = T0; t < T1; ++t, ++tiles_done) {
+      // wait for the epilogue to have drained this accumulator buffer
+      if (!bad && tiles_done >= p.acc_bufs) bad = !mbar_wait(&acc_empty[acc], accph ^ 1u);
+      if (__any_sync(0xFFFFFFFFu, bad)) { bad = true; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.npad);
+      for (int kb0 = 0; kb0 < p.kblocks; kb0 += kStageBlocks) {
+        bad = !mbar_wait(&a_full[as], aph);
+        if (__any_sync(0xFFFFFFFFu, bad)) { bad = true; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.npad);
-        for (int kb = 0; kb < p.kblocks && !bad; ++kb) {
-          bad = !mbar_wait(&a_full[as], aph);
-          if (!bad) {
-            if (p.x_resident) {
-              if (!x_ready) {
-                bad = !mbar_wait(&x_full[0], 0u);
-                x_ready = true;
-              }
-            } else {
-              bad = !mbar_wait(&x_full[xs], xph);
-            }
-          }
-          if (bad) break;
-          tc_fence_after();
-          const uint32_t a_addr = base + p.off_a + as * kABytes;
-          const uint32_t x_addr = p.x_resident ? base + p.off_x + kb * xblock_bytes
-                                               : base + p.off_x + xs * xblock_bytes;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_f16(d_tmem, smem_desc_sw128(a_addr + ks * 32), smem_desc_sw128(x_addr + ks * 32),
-                     idesc, (kb > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(&a_empty[as]);            // A block consumed
-          if (++as == kAStages) { as = 0; aph ^= 1u; }
+        const int nb = min(kStageBlocks, p.kblocks - kb0);
+        const uint64_t ad0 = adesc0 + (uint64_t)as * (kStageBlocks * kAStep);
+        for (int sb = 0; sb < nb; ++sb) {
+          const int kb = kb0 + sb;
           if (!p.x_resident) {
-            umma_commit(&x_empty[xs]);          // activation block consumed
-            if (++xs == p.xstages) { xs = 0; xph ^= 1u; }
+            bad = !mbar_wait(&x_full[xs], xph);
+            if (__any_sync(0xFFFFFFFFu, bad)) { bad = true; break; }
+            tc_fence_after();
           }
+          const uint64_t ad = ad0 + (uint64_t)sb * kAStep;
+          const uint64_t xd = xdesc0 + (uint64_t)(p.x_resident ? kb : xs) * xstep;
+          if (leader) {
+            umma_f16(d_tmem, ad, xd, idesc, kb > 0 ? 1u : 0u);
+            umma_f16(d_tmem, ad + kKStep, xd + kKStep, idesc, 1u);
+            umma_f16(d_tmem, ad + 2 * kKStep, xd + 2 * kKStep, idesc, 1u);
+            umma_f16(d_tmem, ad + 3 * kKStep, xd + 3 * kKStep, idesc, 1u);
+            if (!p.x_resident) umma_commit(&x_empty[xs]);   // activation block consumed
+          }
+          __syncwarp();
+          if (!p.x_resident && ++xs == p.xstages) { xs = 0; xph ^= 1u; }
         }
         if (bad) break;
-        umma_commit(&acc_full[acc]);            // accumulator ready for the epilogue
-        if (++acc == p.acc_bufs) { acc = 0; accph ^= 1u; }
+        if (leader) umma_commit(&a_empty[as]);  // A stage consumed
+        __syncwarp();
+        if (++as == p.astages) { as = 0; aph ^= 1u; }
       }
+      if (bad) break;
+      if (leader) umma_commit(&acc_full[acc]);  // accumulator ready for the epilogue
+      __syncwarp();
+      if (++acc == p.acc_bufs) { acc = 0; accph ^= 1u; }
     }
   } else if (warp < kEpilogueWarp0) {
     // ------------------------------ dequantisers ------------------------------
-    const int tdq = threadIdx.x - kDequantWarp0 * 32;     // 0..255
+    // A stages hold kStageBlocks consecutive 64-column blocks; group g
+    // fills block g of every stage, so a stage is ready after one block's
+    // time.  Stages are numbered js = 0, 1, ... over the CTA's tiles and use
+    // A buffer js % astages.  Each packed chunk holds whole stages; both
+    // groups wait for it and release it.
+    const int dq = warp - kDequantWarp0;                   // 0..15
+    const int grp = dq / kGroupWarps;
+    const int tdq = (dq % kGroupWarps) * 32 + lane;        // 0..255 within the group
     const int r = tdq & (kTileRows - 1);                   // row of the tile
     const int half = tdq >> 7;                             // which 32 codes of a block
     const uint32_t sw = (uint32_t)(r & 7);
-    int ws = 0, as = 0;
-    uint32_t wph = 0, aph = 0;
-    int afills = 0, sfills = 0;
+    int ws = 0;
+    uint32_t wph = 0;
+    int sfills = 0;
+    const int spt = (p.kblocks + kStageBlocks - 1) / kStageBlocks;   // stages per tile
     const int gblocks = a.group_eff / 64;                  // 64-column blocks per group
     for (int t = T0; t < T1; ++t) {
+      const unsigned int js0 = (unsigned int)((t - T0) * spt);
       const int row = min(t * kTileRows + r, n - 1);
       const bool staged = p.sbuf_bytes > 0 && p.scales_aligned && (t + 1) * kTileRows <= n;
       const int slot = sfills & 1;
@@ -347,55 +392,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         srow = a.scales + (size_t)row * p.ngroups;
       }
-      int kb = 0, gi = 0, bin = 0;
-      for (int c = 0; c < p.chunks; ++c) {
-        if (!bad) bad = !mbar_wait(&w_full[ws], wph);
-        const uint32_t wrow = base + p.off_w + ws * kWChunkBytes + r * 128;
-        for (int b = 0; b < kBlocksPerChunk && kb < p.kblocks; ++b, ++kb) {
-          if (afills >= kAStages && !bad) bad = !mbar_wait(&a_empty[as], aph ^ 1u);
-          if (!bad) {
-            const uint16_t sbits = staged ? srow[gi] : ldg_u16(srow + gi);
-            const uint32_t s2 = (uint32_t)sbits | ((uint32_t)sbits << 16);
-            const uint32_t arow = base + p.off_a + as * kABytes + r * 128;
-            if constexpr (BITS == 4) {
-              // 16 packed bytes = 32 codes = A chunks 4*half .. 4*half+3
-              const uint32_t piece = (uint32_t)(2 * b + half) ^ sw;
-              const uint4 v = lds128(wrow + piece * 16);
-              const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int wdi = 0; wdi < 4; ++wdi) {
-                uint32_t o[4];
-                int4_q_times_s(words[wdi], s2, o);
-                const uint32_t chunk = (uint32_t)(4 * half + wdi) ^ sw;
-                st_shared_v4(arow + chunk * 16, o[0], o[1], o[2], o[3]);
-              }
-            } else {
-#pragma unroll
-              for (int h2 = 0; h2 < 2; ++h2) {
-                const int h = 2 * half + h2;                // 16 codes per packed piece
-                const uint32_t piece = (uint32_t)(4 * b + h) ^ sw;
-                const uint4 v = lds128(wrow + piece * 16);
-                uint32_t o0[2], o1[2], o2[2], o3[2];
-                int8_q_times_s(v.x, s2, o0);
-                int8_q_times_s(v.y, s2, o1);
-                int8_q_times_s(v.z, s2, o2);
-                int8_q_times_s(v.w, s2, o3);
-                st_shared_v4(arow + (((uint32_t)(2 * h) ^ sw) * 16), o0[0], o0[1], o1[0], o1[1]);
-                st_shared_v4(arow + (((uint32_t)(2 * h + 1) ^ sw) * 16), o2[0], o2[1], o3[0],
-                             o3[1]);
-              }
-            }
-            fence_async_smem();                 // generic-proxy writes -> tensor core
+      int cur_chunk = -1;
+      for (int st = 0; st < spt; ++st) {
+        const int kb = st * kStageBlocks + grp;            // this group's block
+        const bool have = kb < p.kblocks;                  // (absent in an odd tail stage)
+        // the chunk holding this stage (a stage never spans two chunks)
+        const int c = (st * kStageBlocks) / kBlocksPerChunk;
+        if (c != cur_chunk) {
+          if (cur_chunk >= 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&w_empty[ws]);
+            if (++ws == p.wstages) { ws = 0; wph ^= 1u; }
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[as]);
-          ++afills;
-          if (++as == kAStages) { as = 0; aph ^= 1u; }
-          if (++bin == gblocks) { bin = 0; ++gi; }
+          if (!bad) bad = !mbar_wait(&w_full[ws], wph);
+          cur_chunk = c;
+        }
+        const unsigned int js = js0 + (unsigned int)st;
+        const int as = (int)(js % (unsigned int)p.astages);
+        // the buffer's previous fill (astages stages back) must be consumed
+        if (js >= (unsigned int)p.astages && !bad)
+          bad = !mbar_wait(&a_empty[as], ((js / (unsigned int)p.astages) & 1u) ^ 1u);
+        if (have && !bad) {
+          const int b = kb % kBlocksPerChunk;
+          const uint32_t wrow = base + p.off_w + ws * kWChunkBytes + r * 128;
+          const int gi = kb / gblocks;
+          const uint16_t sbits = staged ? srow[gi] : ldg_u16(srow + gi);
+          const uint32_t s2 = (uint32_t)sbits | ((uint32_t)sbits << 16);
+          const uint32_t arow = base + p.off_a + as * kAStageBytes + grp * kABytes + r * 128;
+          if constexpr (BITS == 4) {
+            // 16 packed bytes = 32 codes = A chunks 4*half .. 4*half+3
+            const uint32_t piece = (uint32_t)(2 * b + half) ^ sw;
+            const uint4 v = lds128(wrow + piece * 16);
+            const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int wdi = 0; wdi < 4; ++wdi) {
+              uint32_t o[4];
+              int4_q_times_s(words[wdi], s2, o);
+              const uint32_t chunk = (uint32_t)(4 * half + wdi) ^ sw;
+              st_shared_v4(arow + chunk * 16, o[0], o[1], o[2], o[3]);
+            }
+          } else {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int h = 2 * half + h2;                // 16 codes per packed piece
+              const uint32_t piece = (uint32_t)(4 * b + h) ^ sw;
+              const uint4 v = lds128(wrow + piece * 16);
+              uint32_t o0[2], o1[2], o2[2], o3[2];
+              int8_q_times_s(v.x, s2, o0);
+              int8_q_times_s(v.y, s2, o1);
+              int8_q_times_s(v.z, s2, o2);
+              int8_q_times_s(v.w, s2, o3);
+              st_shared_v4(arow + (((uint32_t)(2 * h) ^ sw) * 16), o0[0], o0[1], o1[0], o1[1]);
+              st_shared_v4(arow + (((uint32_t)(2 * h + 1) ^ sw) * 16), o2[0], o2[1], o3[0],
+                           o3[1]);
+            }
+          }
+          fence_async_smem();                   // generic-proxy writes -> tensor core
         }
         __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[as]);
+      }
+      if (cur_chunk >= 0) {
+        __syncwarp();
         if (lane == 0) mbar_arrive(&w_empty[ws]);
-        if (++ws == kWStages) { ws = 0; wph ^= 1u; }
+        if (++ws == p.wstages) { ws = 0; wph ^= 1u; }
       }
       if (staged) {
         __syncwarp();
@@ -482,33 +542,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 struct TcLayout {
   uint32_t off_w, off_a, off_x, off_bar, off_s, off_st;
   size_t smem;
-  int x_resident, xstages, sbuf_bytes;
+  int x_resident, xstages, sbuf_bytes, wstages, astages;
 };
 
-TcLayout tc_plan(int npad, int k, int ngroups) {
+// Shared memory: packed-weight ring, A stages, activations (resident for the
+// whole launch when that still leaves a ring of kMinWStages, else a ring of
+// 64-column blocks), then barriers, scale rows and the logits staging.  The
+// weight ring takes what is left, up to kMaxWStages chunks: it is what keeps
+// enough bytes in flight when the kernel is bound by HBM (small m).
+TcLayout tc_plan_a(int npad, int k, int ngroups, int astages) {
   TcLayout L{};
+  L.astages = astages;
   const uint32_t xblock = (uint32_t)npad * 128u;
   const int kblocks = k / 64;
   const uint32_t sbuf = rup((uint32_t)(kTileRows * ngroups * 2), 128u);
   L.sbuf_bytes = (2 * sbuf <= 24u * 1024u) ? (int)sbuf : 0;   // else direct scale loads
   const uint32_t tail = 512 + 128 + 2 * L.sbuf_bytes + 128 + kStageBytes + 128 + 1024;
   const uint32_t limit = 227u * 1024u;
-  uint32_t off = 0;
-  L.off_w = off;
-  off += kWStages * kWChunkBytes;
-  L.off_a = off;
-  off += kAStages * kABytes;
-  L.off_x = off;
+  const uint32_t fixed = (uint32_t)astages * kAStageBytes + tail;
   const uint32_t resident = (uint32_t)kblocks * xblock;
-  if (off + resident + tail <= limit) {
+  uint32_t xbytes;
+  if (fixed + resident + kMinWStages * kWChunkBytes <= limit) {
     L.x_resident = 1;
     L.xstages = 1;
-    off += resident;
+    xbytes = resident;
   } else {
     L.x_resident = 0;
-    L.xstages = (off + 3 * xblock + tail <= limit) ? 3 : 2;
-    off += L.xstages * xblock;
+    L.xstages = (fixed + 3 * xblock + kMinWStages * kWChunkBytes <= limit) ? 3 : 2;
+    xbytes = L.xstages * xblock;
   }
+  const uint32_t room = limit > fixed + xbytes ? limit - fixed - xbytes : 0;
+  L.wstages = (int)(room / kWChunkBytes);
+  if (L.wstages > kMaxWStages) L.wstages = kMaxWStages;
+  uint32_t off = 0;
+  L.off_w = off;
+  off += (uint32_t)L.wstages * kWChunkBytes;
+  L.off_a = off;
+  off += (uint32_t)astages * kAStageBytes;
+  L.off_x = off;
+  off += xbytes;
   L.off_bar = rup(off, 64);
   off = L.off_bar + 512;
   L.off_s = rup(off, 128);
@@ -517,6 +589,16 @@ TcLayout tc_plan(int npad, int k, int ngroups) {
   off = L.off_st + kStageBytes;
   L.smem = off + 1024;
   return L;
+}
+
+// Shared memory: packed-weight ring, A stages, activations (resident for the
+// whole launch when that still leaves a ring of kMinWStages, else a ring of
+// 64-column blocks), then barriers, scale rows and the logits staging.  The
+// weight ring takes what is left, up to kMaxWStages chunks (it keeps bytes
+// in flight when the kernel is bound by HBM).  A third A stage measured no
+// faster than a deeper weight ring at m = 32, and does not fit at m = 256.
+TcLayout tc_plan(int npad, int k, int ngroups) {
+  return tc_plan_a(npad, k, ngroups, kMinAStages);
 }
 
 template <int BITS>
@@ -541,7 +623,8 @@ bool tc_supported(const LogitsArgs& a) {
   if (a.x_dtype != WQL_F16 || a.scale_dtype != WQL_F16) return false;
   if (a.m < 1 || a.m > 256 || a.k % 64 != 0) return false;
   const int npad = (a.m + 15) / 16 * 16;
-  return tc_plan(npad, a.k, a.k / a.group_eff).smem <= 227u * 1024u;
+  const TcLayout L = tc_plan(npad, a.k, a.k / a.group_eff);
+  return L.wstages >= 2 && L.smem <= 227u * 1024u;
 }
 
 cudaError_t launch_tc(const LogitsArgs& a, unsigned int* err, cudaStream_t s) {
@@ -565,6 +648,8 @@ cudaError_t launch_tc(const LogitsArgs& a, unsigned int* err, cudaStream_t s) {
   p.scales_aligned = (reinterpret_cast<uintptr_t>(a.scales) % 16) == 0;
   p.x_resident = L.x_resident;
   p.xstages = L.xstages;
+  p.wstages = L.wstages;
+  p.astages = L.astages;
   p.off_w = L.off_w;
   p.off_a = L.off_a;
   p.off_x = L.off_x;
