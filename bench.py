@@ -410,6 +410,131 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
 
 
 # ---------------------------------------------------------------------------
+# Argmax study: int8 per-row head, M = 1 rows, top-8 rescoring
+# ---------------------------------------------------------------------------
+
+def run_argmax_study(args) -> dict:
+    """The 151936 x 2048 int8 per-row head with an fp16 reference weight
+    ("Fused WNA16 GEMM for tied quantized lm_head logits", reviewer comment
+    items 1-2): 4096 seeded rows, each an M = 1 wql_logits call with top-8
+    followed by wql_topk_rescore from the fp16 rows.  Reports how often the
+    greedy token agrees with the fp16 reference -- the argmax of x . W_fp16
+    computed with exact products and fp32 accumulation (torch matmul of the
+    widened operands) -- for the int8 logits alone and after rescoring, the
+    rows whose reference top-1/top-2 margin is below 2^-10 * sum|x w| (near
+    ties no weight precision decides), and the device time per call.  The
+    pages' own agreement rates come from captured decode states that are not
+    available here; synthetic rows have no comparable argmax structure."""
+    import torch
+    import weight_only_quantized_wql_gb300 as wql
+    from weight_only_quantized_wql_gb300 import synth
+
+    wl = synth.WORKLOADS["qwen_151936x2048_w8row_rescore"]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wql.load()
+    stream = torch.cuda.current_stream(dev)
+    w_ref = synth.weight(wl.n, wl.k, wl.w_dtype, seed=wl.w_seed, device=dev)    # fp16
+    qw = wql.wql_quantize(w_ref, wl.bits, wl.group, torch.float16, wl.clip)
+    xs = synth.activations(wl.rows, wl.k, wl.x_dtype, seed=wl.x_seed, device=dev)
+    # fp16 reference: exact products, fp32 accumulation; the near-tie scale
+    # sum|x w| from the absolute values
+    ref_top = torch.empty(wl.rows, 2, dtype=torch.int64, device=dev)
+    near = torch.empty(wl.rows, dtype=torch.bool, device=dev)
+    wf = w_ref.float()
+    for r0 in range(0, wl.rows, 256):
+        xf = xs[r0:r0 + 256].float()
+        lg = xf @ wf.t()
+        v2, i2 = lg.topk(2, dim=1)
+        ref_top[r0:r0 + 256] = i2
+        absw = (xf.abs() @ wf.abs().t()).gather(1, i2[:, :1]).squeeze(1)
+        near[r0:r0 + 256] = (v2[:, 0] - v2[:, 1]) < absw * 2.0 ** -10
+        del lg
+    del wf
+    B = 16                                    # rows per captured graph replay
+    xbuf = torch.empty(B, wl.k, dtype=torch.float16, device=dev)
+    lbuf = torch.empty(B, wl.n, dtype=torch.float16, device=dev)
+    ibuf = torch.empty(B, wl.rescore_k, dtype=torch.int32, device=dev)
+    vbuf = torch.empty(B, wl.rescore_k, dtype=torch.float32, device=dev)
+    ws = wql.Workspace(dev)
+
+    def rows_fn(rescore):
+        def fn():
+            for i in range(B):
+                wql.wql_logits(xbuf[i:i + 1], qw, topk=wl.rescore_k, workspace=ws,
+                               out=lbuf[i:i + 1], topk_idx=ibuf[i:i + 1],
+                               topk_val=vbuf[i:i + 1])
+                if rescore:
+                    wql.wql_topk_rescore(xbuf[i:i + 1], w_ref, ibuf[i:i + 1],
+                                         vbuf[i:i + 1], lbuf[i:i + 1])
+        return fn
+
+    xbuf.copy_(xs[:B])
+    for _ in range(3):
+        rows_fn(True)()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(dev)
+    graphs = {}
+    for resc in (False, True):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                rows_fn(resc)()
+        stream.wait_stream(cap)
+        graphs[resc] = g
+    top1 = {False: torch.empty(wl.rows, dtype=torch.int64, device=dev),
+            True: torch.empty(wl.rows, dtype=torch.int64, device=dev)}
+    dev_us = {False: 0.0, True: 0.0}
+    for resc in (False, True):
+        for r0 in range(0, wl.rows, B):
+            xbuf.copy_(xs[r0:r0 + B])
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graphs[resc].replay()
+            b.record(stream)
+            # the greedy token of each row: the top candidate of the int8
+            # logits (fp32 values), or after rescoring the argmax over the
+            # whole scattered row
+            top1[resc][r0:r0 + B] = (lbuf.float().argmax(dim=1) if resc
+                                     else ibuf[:, 0].long())
+            torch.cuda.synchronize()
+            dev_us[resc] += a.elapsed_time(b) * 1e3
+    assert ws.error_word() == 0, "a kernel's bounded wait timed out"
+    ref1 = ref_top[:, 0]
+    agree = {resc: int((top1[resc] == ref1).sum()) for resc in (False, True)}
+    n_near = int(near.sum())
+    far = ~near
+    agree_far = {resc: int(((top1[resc] == ref1) & far).sum()) for resc in (False, True)}
+    per_call = dev_us[False] / wl.rows
+    per_pair = dev_us[True] / wl.rows
+    b_logits = logits_bytes(1, wl.n, wl.k, 8, 0, topk=wl.rescore_k)
+    b_pair = b_logits + rescore_bytes(1, wl.k, wl.rescore_k)
+    pk = peaks()
+    return {
+        "study": "argmax agreement, int8 per-row lm_head 151936x2048 + top-8 rescore from "
+                 "fp16 rows, 4096 seeded M=1 rows",
+        "data": "synthetic",
+        "rows": wl.rows,
+        "agree_int8": agree[False], "agree_rescored": agree[True],
+        "agree_int8_frac": round(agree[False] / wl.rows, 5),
+        "agree_rescored_frac": round(agree[True] / wl.rows, 5),
+        "near_tie_rows": n_near,
+        "agree_int8_excl_near_ties": agree_far[False],
+        "agree_rescored_excl_near_ties": agree_far[True],
+        "rows_excl_near_ties": wl.rows - n_near,
+        "us_per_call_logits_top8": round(per_call, 2),
+        "GBps_logits_top8": round(b_logits / (per_call * 1e-6) / 1e9, 1),
+        "frac_hbm_logits_top8": round(b_logits / (per_call * 1e-6) / 1e9 / pk["hbm_gbs"], 3),
+        "us_per_call_with_rescore": round(per_pair, 2),
+        "GBps_with_rescore": round(b_pair / (per_pair * 1e-6) / 1e9, 1),
+        "timing": "device: CUDA-graph replays of 16 consecutive rows (one call pair per "
+                  "row), events around each replay",
+        "reference": "argmax of x . W_fp16 with exact products and fp32 accumulation",
+    }
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle arm (cpu_baseline and --impl reference)
 # ---------------------------------------------------------------------------
 
@@ -505,6 +630,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--study", choices=["argmax"], default=None,
+                    help="argmax: the int8 per-row head's greedy-token agreement study "
+                         "(a separate JSON line, not the bench line)")
     ap.add_argument("--ms", type=int, nargs="+", default=list(MS),
                     help="token counts M timed per step (default: 1 32 256); a subset "
                          "is for profiling one call, not a bench line")
@@ -513,6 +641,11 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.study == "argmax":
+        if rank == 0:
+            print(json.dumps(run_argmax_study(args)), flush=True)
+        return 0
 
     if args.impl == "reference":
         if rank == 0:

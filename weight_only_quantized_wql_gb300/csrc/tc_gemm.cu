@@ -392,6 +392,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         srow = a.scales + (size_t)row * p.ngroups;
       }
+      // The scale of this group's block in each of the tile's stages,
+      // preloaded (stage st's in half st & 1 of sk[st >> 1]) when a row has 8
+      // or 16 groups and a tile at most 8 stages: one or two 16-byte loads
+      // of the row instead of a 2-byte load per block, whose 16- or 32-byte
+      // row stride puts 4 or 8 rows of a warp on one shared-memory bank.
+      const bool pre = spt <= 8 && (p.ngroups == 8 || p.ngroups == 16) && gblocks <= 2 &&
+                       (staged || p.scales_aligned);
+      uint32_t sk[4] = {0u, 0u, 0u, 0u};
+      if (pre && !bad) {
+        uint32_t wv[8];
+        const uint4* src = reinterpret_cast<const uint4*>(srow);
+        const uint4 v0 = staged ? src[0] : __ldg(src);
+        const uint4 v1 = p.ngroups == 16 ? (staged ? src[1] : __ldg(src + 1)) : v0;
+        wv[0] = v0.x; wv[1] = v0.y; wv[2] = v0.z; wv[3] = v0.w;
+        wv[4] = v1.x; wv[5] = v1.y; wv[6] = v1.z; wv[7] = v1.w;
+        if (gblocks == 2) {
+          // stage st uses group st: words 0..3 as they are
+          sk[0] = wv[0]; sk[1] = wv[1]; sk[2] = wv[2]; sk[3] = wv[3];
+        } else {
+          // stage st uses group 2 st + grp: half grp of word st, paired up
+          const uint32_t sel = grp ? 0x7632u : 0x5410u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sk[j] = prmt(wv[2 * j], wv[2 * j + 1], sel);
+        }
+      }
       int cur_chunk = -1;
       for (int st = 0; st < spt; ++st) {
         const int kb = st * kStageBlocks + grp;            // this group's block
@@ -415,8 +440,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (have && !bad) {
           const int b = kb % kBlocksPerChunk;
           const uint32_t wrow = base + p.off_w + ws * kWChunkBytes + r * 128;
-          const int gi = kb / gblocks;
-          const uint16_t sbits = staged ? srow[gi] : ldg_u16(srow + gi);
+          uint16_t sbits;
+          if (pre) {
+            const int q = st >> 1;
+            const uint32_t wsel = q == 0 ? sk[0] : q == 1 ? sk[1] : q == 2 ? sk[2] : sk[3];
+            sbits = (uint16_t)((st & 1) ? (wsel >> 16) : (wsel & 0xFFFFu));
+          } else {
+            const int gi = kb / gblocks;
+            sbits = staged ? srow[gi] : ldg_u16(srow + gi);
+          }
           const uint32_t s2 = (uint32_t)sbits | ((uint32_t)sbits << 16);
           const uint32_t arow = base + p.off_a + as * kAStageBytes + grp * kABytes + r * 128;
           if constexpr (BITS == 4) {
