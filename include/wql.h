@@ -177,8 +177,8 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m,
  *     before any stream capture begins.  A failed setup returns WQL_ECUDA and
  *     is retried by the next call.
  *   - The area's first 256 bytes (ticket counter, error word, per-token
- *     top-K bounds) are cleared on `stream` at the start of every call (one
- *     small memset before the launches).
+ *     top-K bounds and candidate counts) are cleared on `stream` at the
+ *     start of every call (one small memset before the launches).
  *   - Calls on one device share the area: calls that may be in flight at
  *     the same time (other streams, unsynchronised host threads) race and
  *     corrupt each other's outputs.  Serialise them.

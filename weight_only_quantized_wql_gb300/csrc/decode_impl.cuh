@@ -30,9 +30,12 @@
 //    they do not fit, a global scratch row).  Each CTA takes a threshold per
 //    token -- the K-th largest of each warp's lane maxima, a lower bound of
 //    the K-th largest value -- keeps the rows at or above it and selects its
-//    top-K from those; it also raises a per-token global bound with its K-th
-//    value.  The last CTA to finish (atomic ticket, no waiting) keeps the
-//    CTAs' candidates at or above that bound and selects the final top-K.
+//    top-K from those; it raises a per-token global bound with its K-th
+//    value and appends those of its K that reach the bound (as it stands
+//    after its own raise) to a per-token list in the workspace.  The last
+//    CTA to finish (atomic ticket, no waiting) ranks that short list: every
+//    entry of the final top-K reaches the final bound, hence the bound at
+//    its CTA's append, so it is on the list.
 //  * All mbarrier waits are bounded; a timeout sets the workspace error word
 //    and the CTA finishes without issuing further copies.
 #pragma once
@@ -58,6 +61,7 @@ constexpr int kMaxTok = 16;
 constexpr int kConsumerBarrier = 1;              // named barrier for the consumer warps
 constexpr int kSelCap = 256;                     // candidate slots per token in the selection
 constexpr int kTauWord = 16;                     // workspace word of token 0's global bound
+constexpr int kNCandWord = 32;                   // workspace word of token 0's candidate count
 
 struct DecodeParams {
   LogitsArgs a;
@@ -89,9 +93,6 @@ struct SelWork {
   unsigned long long cand[kMaxTok][kSelCap];   // the kept keys
 };
 static_assert(sizeof(SelWork) <= (size_t)kStages * kStageWBytes, "selection area > ring");
-// the rest of the ring stages the CTAs' candidates for the final merge
-constexpr size_t kStageKeyOff = (sizeof(SelWork) + 127) / 128 * 128;
-constexpr size_t kStageKeyBytes = (size_t)kStages * kStageWBytes - kStageKeyOff;
 
 __host__ __device__ constexpr uint32_t round_up_u32(uint32_t v, uint32_t a) {
   return (v + a - 1) / a * a;
@@ -141,6 +142,12 @@ __device__ __forceinline__ void select_topk(int m, int K, int count, unsigned lo
     warp_merge_topk_redux<KT>(l2, K, out);
     out_tok = warp;
   }
+}
+
+__device__ __forceinline__ unsigned long long shfl_u64(unsigned long long v, int src) {
+  const uint32_t lo = __shfl_sync(0xFFFFFFFFu, (uint32_t)v, src);
+  const uint32_t hi = __shfl_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), src);
+  return ((unsigned long long)hi << 32) | lo;
 }
 
 // Order-preserving 32-bit key of a value (the high half of topk_key): NaN 0.
@@ -322,7 +329,7 @@ template <int KT, typename XT, bool kSmemVals>
 __device__ __noinline__ void topk_tail(const DecodeParams& p, SelWork& W,
                                           unsigned long long* red, unsigned int* flags,
                                           int nunits, const int* blk_list, bool cta_bad,
-                                          const float* svals, unsigned long long* stage_keys) {
+                                          const float* svals) {
   const LogitsArgs& a = p.a;
   unsigned int* err = p.err;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -351,11 +358,27 @@ __device__ __noinline__ void topk_tail(const DecodeParams& p, SelWork& W,
       select_topk<KT>(m, K, count, red, key, best, tok);
       res = lane_slot_of_list<KT>(best, K);
     }
-    if (tok >= 0 && res.slot >= 0) {
-      a.cand[((size_t)tok * WQL_MAX_CTAS + blockIdx.x) * K + res.slot] = res.key;
-      // every CTA's K-th value bounds the final K-th value from below
-      if (res.slot == K - 1 && res.key != kEmptyKey)
-        atomicMax(tau + tok, (uint32_t)(res.key >> 32));
+    if (tok >= 0) {
+      // every CTA's K-th value bounds the final K-th value from below: raise
+      // the token's bound, then append this CTA's entries that reach it as
+      // it stands after the raise (the reply of the atomic) -- an entry of
+      // the final top K reaches the final bound, hence this one, and the
+      // list stays short because later CTAs see an ever higher bound
+      const unsigned int kth_lane = __ballot_sync(0xFFFFFFFFu, res.slot == K - 1);
+      unsigned long long kth_key = shfl_u64(res.key, kth_lane ? __ffs(kth_lane) - 1 : 0);
+      if (kth_lane == 0u) kth_key = kEmptyKey;
+      uint32_t bound = 0u;
+      if (lane == 0 && kth_key != kEmptyKey)
+        bound = max(atomicMax(tau + tok, (uint32_t)(kth_key >> 32)), (uint32_t)(kth_key >> 32));
+      bound = __shfl_sync(0xFFFFFFFFu, bound, 0);
+      const bool pass = res.slot >= 0 && res.key != kEmptyKey && (uint32_t)(res.key >> 32) >= bound;
+      const unsigned int pm = __ballot_sync(0xFFFFFFFFu, pass);
+      unsigned int at = 0u;
+      if (lane == 0 && pm != 0u) at = atomicAdd(a.counter + kNCandWord + tok, (unsigned int)__popc(pm));
+      at = __shfl_sync(0xFFFFFFFFu, at, 0);
+      // at most K per CTA: the list never outgrows its WQL_MAX_CTAS * K slots
+      if (pass)
+        a.cand[(size_t)tok * WQL_MAX_CTAS * K + at + __popc(pm & ((1u << lane) - 1u))] = res.key;
     }
   }
   __syncthreads();
@@ -363,63 +386,45 @@ __device__ __noinline__ void topk_tail(const DecodeParams& p, SelWork& W,
   __syncthreads();
   if (flags[1] == 0u) return;
   // The error word (set by any CTA whose bounded wait timed out, before its
-  // ticket): its load is in flight during the staging; with an error the
-  // results are replaced by "no entries" at the end.  A CTA that timed out
-  // itself skips the staging (copies of its own may still land in the ring).
+  // ticket): with an error the results are replaced by "no entries".  A CTA
+  // that timed out itself reports no entries directly.
   const unsigned int errv = __ldcg(err);
   if (!cta_bad) {
-    // the CTAs' candidates, staged in shared memory a group of tokens at a time
-    const int count = (int)gridDim.x * K;
-    const int group = max(1, min(m, (int)(kStageKeyBytes / ((size_t)count * 8))));
-    for (int t0 = 0; t0 < m; t0 += group) {
-      const int mg = min(group, m - t0);
-      // eight loads in flight per thread
-      const int total = mg * count;
-      if (mg == 1) {
-        const unsigned long long* src = a.cand + (size_t)t0 * WQL_MAX_CTAS * K;
-        for (int i0 = threadIdx.x; i0 < count; i0 += 8 * (int)blockDim.x) {
-          unsigned long long v[8];
-#pragma unroll
-          for (int b = 0; b < 8; ++b) v[b] = __ldcg(src + min(i0 + b * (int)blockDim.x, count - 1));
-#pragma unroll
-          for (int b = 0; b < 8; ++b)
-            if (i0 + b * (int)blockDim.x < count) stage_keys[i0 + b * (int)blockDim.x] = v[b];
-        }
-      } else
-      for (int i0 = threadIdx.x; i0 < total; i0 += 8 * (int)blockDim.x) {
-        unsigned long long v[8];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const int i = min(i0 + b * (int)blockDim.x, total - 1);
-          const int tl = i / count;
-          v[b] = __ldcg(a.cand + (size_t)(t0 + tl) * WQL_MAX_CTAS * K + (i - tl * count));
-        }
-#pragma unroll
-        for (int b = 0; b < 8; ++b)
-          if (i0 + b * (int)blockDim.x < total) stage_keys[i0 + b * (int)blockDim.x] = v[b];
-      }
-      if (threadIdx.x < mg) {
-        W.thr[threadIdx.x] = __ldcg(tau + t0 + threadIdx.x);
-        W.cnt[threadIdx.x] = 0u;
-      }
-      __syncthreads();
-      auto key = [&](int tl, int i) { return stage_keys[tl * count + i]; };
-      auto vkey = [&](int tl, int i) { return (uint32_t)(stage_keys[tl * count + i] >> 32); };
+    // warp t ranks token t's appended candidates (m <= kMaxTok < warps)
+    if (warp < m) {
+      const unsigned long long* list = a.cand + (size_t)warp * WQL_MAX_CTAS * K;
+      // the first 32 slots are read together with the count (slots beyond
+      // it hold older entries and are masked): one round trip, not two
+      const unsigned long long first = __ldcg(list + lane);
+      const int c = (int)__ldcg(a.counter + kNCandWord + warp);
       LaneSlot res{kEmptyKey, -1};
-      int tok;
-      if (!cta_topk<KT>(mg, K, count, vkey, key, W, res, tok)) {
-        unsigned long long best[KT];
-        select_topk<KT>(mg, K, count, red, key, best, tok);
-        res = lane_slot_of_list<KT>(best, K);
+      if (c <= 32) {
+        res = warp_rank_of_32(lane < c ? first : kEmptyKey, c, K);
+      } else {
+        unsigned long long best[KT], out[KT];
+#pragma unroll
+        for (int i = 0; i < KT; ++i) best[i] = kEmptyKey;
+        for (int i0 = lane; i0 < c; i0 += 8 * 32) {
+          unsigned long long v[8];   // eight loads in flight per lane
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const int i = i0 + 32 * b;
+            v[b] = i < c ? __ldcg(list + i) : kEmptyKey;
+          }
+#pragma unroll
+          for (int b = 0; b < 8; ++b) list_insert<KT>(best, v[b]);
+        }
+        warp_merge_topk_redux<KT>(best, K, out);
+        res = lane_slot_of_list<KT>(out, K);
       }
-      if (tok >= 0 && res.slot >= 0) {
+      if (res.slot >= 0) {
         const bool ok = errv == 0u && res.key != kEmptyKey;
-        const size_t o = (size_t)(t0 + tok) * K + res.slot;
+        const size_t o = (size_t)warp * K + res.slot;
         a.topk_idx[o] = ok ? key_index(res.key) : -1;
         a.topk_val[o] = ok ? key_value(res.key) : __int_as_float(0x7FC00000);
       }
-      __syncthreads();
     }
+    __syncthreads();
   } else {
     // this CTA timed out: report no entries
     for (int i = threadIdx.x; i < m * K; i += blockDim.x) {
@@ -428,7 +433,10 @@ __device__ __noinline__ void topk_tail(const DecodeParams& p, SelWork& W,
     }
   }
   if (threadIdx.x == 0) *a.counter = 0u;       // ready for the next call
-  if (threadIdx.x < m) tau[threadIdx.x] = 0u;
+  if (threadIdx.x < m) {
+    tau[threadIdx.x] = 0u;
+    a.counter[kNCandWord + threadIdx.x] = 0u;
+  }
 }
 
 // The offset sum of one 16-byte piece of 8 activations: off * sum(x); with
@@ -832,17 +840,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   SelWork& W = *reinterpret_cast<SelWork*>(sm);
   const float* sv = p.vals_stride > 0 ? svals : nullptr;
   const int nunits = (int)flags[2];
-  unsigned long long* stage_keys = reinterpret_cast<unsigned long long*>(sm + kStageKeyOff);
   if (sv) {
     if (a.topk <= 8)
-      topk_tail<8, XT, true>(p, W, red, flags, nunits, blk_list, cta_bad, sv, stage_keys);
+      topk_tail<8, XT, true>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
     else
-      topk_tail<16, XT, true>(p, W, red, flags, nunits, blk_list, cta_bad, sv, stage_keys);
+      topk_tail<16, XT, true>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
   } else {
     if (a.topk <= 8)
-      topk_tail<8, XT, false>(p, W, red, flags, nunits, blk_list, cta_bad, sv, stage_keys);
+      topk_tail<8, XT, false>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
     else
-      topk_tail<16, XT, false>(p, W, red, flags, nunits, blk_list, cta_bad, sv, stage_keys);
+      topk_tail<16, XT, false>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
   }
 }
 

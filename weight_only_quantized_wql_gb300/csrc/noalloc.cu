@@ -13,9 +13,9 @@
 // entry point itself allocates nothing, and neither does anything it calls.
 //
 // What the area holds (the decode kernel's workspace, for at most 16 token
-// rows per launch): the ticket counter, the sticky error word and the
-// per-token top-K bounds (one 256-byte block), the per-CTA top-K candidates,
-// and the fp32 logits that the top-K selection reads back when they do not
+// rows per launch): the ticket counter, the sticky error word, the
+// per-token top-K bounds and candidate counts (one 256-byte block), the top-K
+// candidates, and the fp32 logits that the top-K selection reads back when they do not
 // fit in shared memory.  The 256-byte block must be zero when a launch
 // starts; every call clears it on its own stream before its first launch.  The rest is
 // written before it is read within each launch.
@@ -114,8 +114,8 @@ extern "C" wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t
   unsigned char* ws = static_cast<unsigned char*>(area);
   unsigned int* counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
   unsigned int* err_word = counter + 1;
-  // The counter block (ticket counter, error word, per-token top-K bounds)
-  // starts every call at zero.
+  // The counter block (ticket counter, error word, per-token top-K bounds and
+  // candidate counts) starts every call at zero.
   e = cudaMemsetAsync(counter, 0, 256, stream);
   if (e != cudaSuccess) return record_cuda_error(e);
 
