@@ -546,6 +546,63 @@ def run_argmax_study(args) -> dict:
     }
 
 
+def run_embed_study(args) -> dict:
+    """Tied-embedding gather from the 151936 x 1024 W4-g64 head ("Fused
+    WNA16 GEMM for tied quantized lm_head logits", Purpose): t seeded token
+    ids -> [t, 1024] fp16 rows.  Bytes per call: the ids, each id's packed
+    row and scale row, and the fp16 output; CUDA-graph replays of 20 calls,
+    events around each replay."""
+    import torch
+    import weight_only_quantized_wql_gb300 as wql
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wql.load()
+    stream = torch.cuda.current_stream(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    w = torch.randn(N_VOCAB, K_HIDDEN, generator=gen, device=dev).mul_(0.02)
+    qw = wql.wql_quantize(w, 4, GROUP, torch.float16, wql.CLIP_RTN)
+    del w
+    R = 20
+    pk = peaks()
+    res = {"study": "tied-embedding gather, lm_head 151936x1024 W4-g64 fp16 scales -> fp16 "
+                    "rows", "data": "synthetic", "calls": {}}
+    cap = torch.cuda.Stream(dev)
+    for t in (4096, 65536):
+        ids = torch.randint(0, N_VOCAB, (t,), generator=gen, device=dev, dtype=torch.int32)
+        out = torch.empty(t, K_HIDDEN, dtype=torch.float16, device=dev)
+        for _ in range(3):
+            wql.wql_embed_gather(ids, qw, out=out)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for _ in range(R):
+                    wql.wql_embed_gather(ids, qw, out=out)
+        stream.wait_stream(cap)
+        g.replay()
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            per.append(a.elapsed_time(b) * 1e3 / R)
+        us = statistics.median(per)
+        nbytes = t * (4 + K_HIDDEN // 2 + (K_HIDDEN // GROUP) * 2 + K_HIDDEN * 2)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res["calls"][f"T{t}"] = {"us_median": round(us, 2), "bytes": nbytes,
+                                 "GBps": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)}
+    res["timing"] = "device: CUDA-graph replays of 20 calls, events around each replay"
+    res["note"] = ("4096 ids move 10.7 MB, which L2 absorbs; 65536 ids move 171 MB (the "
+                   "output alone exceeds L2)")
+    return res
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle arm (cpu_baseline and --impl reference)
 # ---------------------------------------------------------------------------
@@ -647,9 +704,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--study", choices=["argmax"], default=None,
-                    help="argmax: the int8 per-row head's greedy-token agreement study "
-                         "(a separate JSON line, not the bench line)")
+    ap.add_argument("--study", choices=["argmax", "embed"], default=None,
+                    help="argmax: the int8 per-row head's greedy-token agreement study; "
+                         "embed: the tied-embedding gather (each a separate JSON line, "
+                         "not the bench line)")
     ap.add_argument("--ms", type=int, nargs="+", default=list(MS),
                     help="token counts M timed per step (default: 1 32 256); a subset "
                          "is for profiling one call, not a bench line")
@@ -659,9 +717,10 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
-    if args.study == "argmax":
+    if args.study is not None:
         if rank == 0:
-            print(json.dumps(run_argmax_study(args)), flush=True)
+            fn = run_argmax_study if args.study == "argmax" else run_embed_study
+            print(json.dumps(fn(args)), flush=True)
         return 0
 
     if args.impl == "reference":

@@ -209,6 +209,24 @@ wql_status wql_topk_rescore(const void* x, int32_t x_dtype, int64_t m,
                             int32_t* topk_idx, float* topk_val,
                             void* logits_inout, cudaStream_t stream);
 
+/* Tied-embedding gather ("Fused WNA16 GEMM for tied quantized lm_head
+ * logits", Purpose: the tied head's quantised weight also serves as the input
+ * embedding, so a token's embedding row is that row of dequant(Wq)).
+ *   ids        device int32 [t]; an id outside [0, n) yields a row of +0
+ *   t          number of ids (0: nothing is launched)
+ *   w          quantised weight (host struct; its pointers are device), the
+ *              same one wql_logits reads
+ *   out_dtype  WQL_F16 or WQL_BF16 (independent of the scale dtype)
+ *   out        device [t, k] of out_dtype, 16-byte aligned (caller-owned):
+ *              out[i, j] = RN_out(q[ids[i], j] * s[ids[i], j / group]), the
+ *              product exact in fp32 and rounded once, to nearest-even
+ * k % 8 == 0, k % group == 0; ids 4-byte and qweight 8-byte aligned.
+ * Errors: WQL_EINVAL for NULL pointers with t > 0 or a malformed weight,
+ * WQL_EUNSUPPORTED for other bit widths, dtypes, sizes or alignments;
+ * asynchronous on `stream`, allocates nothing. */
+wql_status wql_embed_gather(const int32_t* ids, int64_t t, const wql_weight* w,
+                            int32_t out_dtype, void* out, cudaStream_t stream);
+
 /* Static text for a status code. */
 const char* wql_status_string(wql_status status);
 

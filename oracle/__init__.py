@@ -20,6 +20,9 @@ it with numpy arrays.  Each wrapper names the page section it follows:
 * ``logits``     -- same page, Purpose: logits = X . dequant(Wq)^T, the dense
   weight never needed; binary64, k ascending.
 * ``topk`` / ``rescore`` -- same page, reviewer comment item 2.
+* ``embed_gather`` -- same page, Purpose (tied head: a token's input
+  embedding is that row of the dequantised weight), rounded once to
+  fp16 / bf16.
 """
 from __future__ import annotations
 
@@ -83,6 +86,8 @@ def _load():
                                       vp, i32, vp, i64, vp, vp, i32]
         lib.oracle_topk.restype = i32
         lib.oracle_topk.argtypes = [vp, i64, i64, i32, vp, vp]
+        lib.oracle_embed_gather.restype = i32
+        lib.oracle_embed_gather.argtypes = [vp, i64, vp, i32, vp, i32, i64, i64, i64, i32, vp]
         lib.oracle_rescore.restype = i32
         lib.oracle_rescore.argtypes = [vp, i32, i64, i64, vp, i32, i64, vp, i32, vp, i32, vp, vp]
         _lib = lib
@@ -241,6 +246,22 @@ def rescore(x: np.ndarray, x_dtype: int, wref: np.ndarray, wref_dtype: int,
     if rc != 0:
         raise ValueError("oracle_rescore: index out of range")
     return out, absout
+
+
+def embed_gather(ids: np.ndarray, qweight: np.ndarray, bits: int, scales: np.ndarray,
+                 scale_dtype: int, group: int, n: int, k: int, out_dtype: int) -> np.ndarray:
+    """uint16 bits [t, k] of RN_out(q * s) for rows ids (ids outside [0, n): +0)."""
+    lib = _load()
+    ii = np.ascontiguousarray(ids, dtype=np.int32).ravel()
+    qw = np.ascontiguousarray(qweight)
+    sc = np.ascontiguousarray(scales).view(np.uint16)
+    g = k if group == 0 else group
+    out = np.empty((ii.shape[0], k), dtype=np.uint16)
+    rc = lib.oracle_embed_gather(_ptr(ii), ii.shape[0], _ptr(qw), bits, _ptr(sc), scale_dtype,
+                                 g, n, k, out_dtype, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_embed_gather rejected its arguments")
+    return out
 
 
 def tolerance(absacc: np.ndarray) -> np.ndarray:

@@ -459,3 +459,44 @@ int oracle_rescore(const void* x, int x_dtype, int64_t m, int64_t k,
     }
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Tied-embedding gather ("Fused WNA16 GEMM for tied quantized lm_head       */
+/* logits", Purpose: the tied head's quantised weight is also the input      */
+/* embedding, so a token's embedding row is that row of dequant(Wq)).        */
+/* out[i, kk] = RN_out(q[ids[i], kk] * s[ids[i], kk / group]); the product   */
+/* is taken in binary64 (exact: an 8-bit code times an 11- or 8-bit scale)   */
+/* and rounded once to fp16 / bf16, ties to even.  An id outside [0, n)     */
+/* gives a row of +0.  out: t*k storage-dtype bits.                          */
+/* ------------------------------------------------------------------------ */
+int oracle_embed_gather(const int32_t* ids, int64_t t, const void* qweight, int bits,
+                        const uint16_t* scales, int scale_dtype, int64_t group, int64_t n,
+                        int64_t k, int out_dtype, uint16_t* out) {
+  if ((bits != 4 && bits != 8) || group <= 0 || k % group != 0 || k % 8 != 0) return -1;
+  if (out_dtype != OR_F16 && out_dtype != OR_BF16) return -1;
+  const int64_t ng = k / group;
+  for (int64_t i = 0; i < t; ++i) {
+    const int64_t row = ids[i];
+    for (int64_t kk = 0; kk < k; ++kk) {
+      double v = 0.0;
+      if (row >= 0 && row < n) {
+        int q;
+        if (bits == 4) {
+          const uint32_t word = ((const uint32_t*)qweight)[row * (k / 8) + kk / 8];
+          q = (int)((word >> (4 * nibble_pos((int)(kk % 8)))) & 15u) - 8;
+        } else {
+          q = (int)((const int8_t*)qweight)[row * k + kk];
+        }
+        v = (double)q * scale_value(scales[row * ng + kk / group], scale_dtype);
+      }
+      if (out_dtype == OR_F16) {
+        double r = round_to_format(v, 11, -14, 15);
+        out[i * k + kk] = encode_format(copysign(r, v), 11, -14, 15, 5);
+      } else {
+        double r = round_to_format(v, 8, -126, 127);
+        out[i * k + kk] = encode_format(copysign(r, v), 8, -126, 127, 8);
+      }
+    }
+  }
+  return 0;
+}

@@ -107,3 +107,29 @@ def test_quantize_pack_rescore_argument_checks(lib):
     assert r(A, 1, 2, A, 1, 4, 256, None, 8, A, A, A, None) == EINVAL          # topk > n
     assert r(A, 1, 2, A, 1, 100, 256, None, 0, A, A, A, None) == OK            # nothing to do
     assert wql.wql_launch_count() == before
+
+
+def test_embed_gather_argument_checks(lib):
+    before = wql.wql_launch_count()
+    e = lib.wql_embed_gather
+
+    def call(w, ids=A, t=4, odt=1, out=A):
+        return e(ids, t, ctypes.byref(w) if w is not None else None, odt, out, None)
+
+    assert call(None) == EINVAL
+    assert call(_weight(), t=-1) == EINVAL
+    assert call(_weight(reserved=1)) == EINVAL
+    assert call(_weight(), ids=None) == EINVAL
+    assert call(_weight(), out=None) == EINVAL
+    assert call(_weight(s=None)) == EINVAL
+    assert call(_weight(bits=2)) == EUNSUPPORTED
+    assert call(_weight(), odt=0) == EUNSUPPORTED                # fp32 output
+    assert call(_weight(sdt=0)) == EUNSUPPORTED
+    assert call(_weight(k=260, group=0)) == EUNSUPPORTED         # k % 8
+    assert call(_weight(group=24, k=512)) == EUNSUPPORTED        # k % group
+    assert call(_weight(), out=A + 8) == EUNSUPPORTED            # out not 16-byte aligned
+    assert call(_weight(q=A + 4)) == EUNSUPPORTED                # qweight not 8-byte aligned
+    assert call(_weight(), ids=A + 2) == EUNSUPPORTED
+    assert call(_weight(), t=0) == OK                            # nothing launched
+    assert call(_weight(), t=0, ids=None, out=None) == OK
+    assert wql.wql_launch_count() == before

@@ -167,3 +167,22 @@ def test_fullsize_int8_row_rescore():
         # the candidates, up to values the reference dot cannot separate
         best = int(np.argmax(o_val[0]))
         assert o_val[0, 0] >= o_val[0, best] - oracle.tolerance(o_abs[0, best])
+
+
+@pytest.mark.parametrize("name", ["qwen_151936x1024_w4g64", "qwen_151936x1024_w8g128",
+                                  "head_248320x5120_w4g128_mse"])
+def test_fullsize_embed_gather(name):
+    """Tied-embedding gather from the full head: 4096 seeded ids (and the
+    first and last rows), bit-exact against the oracle's gather."""
+    wl, w_host, qw, o_qw, o_s = _quantised(name)
+    gen = torch.Generator().manual_seed(77)
+    ids = torch.cat([torch.tensor([0, wl.n - 1], dtype=torch.int32),
+                     torch.randint(0, wl.n, (4096,), generator=gen, dtype=torch.int32)])
+    odt = wl.x_dtype
+    out = wql.wql_embed_gather(ids.to(DEV), qw, out_dtype=TORCH_OF[odt])
+    torch.cuda.synchronize()
+    want = oracle.embed_gather(ids.numpy(), o_qw, wl.bits, o_s, wl.scale_dtype, wl.group,
+                               wl.n, wl.k, odt)
+    got = np_bits(out)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} outputs differ, first at {bad[:3].tolist()}"

@@ -272,3 +272,39 @@ def test_tensor_core_topk_adversarial_orders(m, order):
     if order == "equal":
         # every row's logit is the same number: value ties go to the lowest indices
         assert (g_idx == np.arange(K)[None, :]).all(), g_idx[:2]
+
+
+@pytest.mark.parametrize("scheme", SCHEMES, ids=lambda s: f"w{s[0]}g{s[1]}s{s[2]}")
+@pytest.mark.parametrize("odt", [oracle.F16, oracle.BF16], ids=["f16", "bf16"])
+def test_embed_gather_bit_exact(scheme, odt):
+    """Tied-embedding gather: rows of the dequantised head for token ids,
+    bit-exact against the oracle; duplicates, the first and last rows, and
+    ids outside [0, n) (rows of zeros)."""
+    n, k = 1000, 320 if scheme[1] in (0, 64) else 512
+    bits, group, sdt, wdt, xdt, clip = scheme
+    w, qw, o_qw, o_s = _make(n, k, scheme, seed=41)
+    gen = torch.Generator().manual_seed(9)
+    ids = torch.cat([torch.tensor([0, n - 1, 5, 5, -1, n, n + 7, -2147483648, 2147483647],
+                                  dtype=torch.int32),
+                     torch.randint(0, n, (300,), generator=gen, dtype=torch.int32)])
+    out = wql.wql_embed_gather(ids.to(DEV), qw, out_dtype=TORCH_OF[odt])
+    torch.cuda.synchronize()
+    want = oracle.embed_gather(ids.numpy(), o_qw, bits, o_s, sdt, group, n, k, odt)
+    assert out.shape == (ids.numel(), k) and out.dtype == TORCH_OF[odt]
+    got = np_bits(out)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} outputs differ, first at {bad[:3].tolist()}"
+
+
+def test_embed_gather_shapes():
+    n, k = 300, 256
+    w, qw, o_qw, o_s = _make(n, k, SCHEMES[0])
+    ids = torch.randint(0, n, (2, 3), generator=torch.Generator().manual_seed(2),
+                        dtype=torch.int32)
+    out = wql.wql_embed_gather(ids.to(DEV), qw)
+    empty = wql.wql_embed_gather(torch.empty(0, dtype=torch.int32, device=DEV), qw)
+    torch.cuda.synchronize()
+    assert out.shape == (2, 3, k) and empty.shape == (0, k)
+    want = oracle.embed_gather(ids.reshape(-1).numpy(), o_qw, 4, o_s, oracle.F16, 64, n, k,
+                               oracle.F16)
+    assert np.array_equal(np_bits(out.reshape(6, k)), want)

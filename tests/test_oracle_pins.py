@@ -7,7 +7,10 @@
   scale, closed-form invariants and exact-arithmetic MSE minimality;
 * logits against a dense numpy fp64 product built before packing, and closed
   forms (unit vectors, zero weight, one live group, constant codes);
-* top-K against a numpy lexsort brute force; rescoring against numpy dots.
+* top-K against a numpy lexsort brute force; rescoring against numpy dots;
+* the tied-embedding gather against a hand-worked word, numpy / torch
+  rounding of products formed from the codes before packing, and its
+  out-of-range and overflow cases.
 """
 from fractions import Fraction
 import os
@@ -371,3 +374,56 @@ def test_rescore_matches_numpy_dot(oracle_mod):
     idx[:, 0] = 17
     out, _ = oracle.rescore(x, F16, wref, F16, idx)
     assert np.all(np.argmax(out, axis=1) == 0)
+
+
+# --------------------------------------------------------------------------
+# tied-embedding gather
+# --------------------------------------------------------------------------
+
+def test_embed_gather_worked_example(oracle_mod):
+    # codes -8..-1 in elements 0..7: nibbles 0..7, even elements in the low
+    # half (0x6420), odd in the high half (0x7531); scale 0.5
+    word = np.array([[0x75316420]], dtype=np.uint32).view(np.int32)
+    scale = np.array([[0x3800]], dtype=np.uint16)            # fp16 0.5
+    out = oracle.embed_gather(np.array([0]), word, 4, scale, F16, 8, 1, 8, F16)
+    want = [0xC400, 0xC300, 0xC200, 0xC100, 0xC000, 0xBE00, 0xBC00, 0xB800]   # -4 .. -0.5
+    assert out[0].tolist() == want
+
+
+@pytest.mark.parametrize("bits,group,sdt,odt", [(4, 64, F16, F16), (4, 128, BF16, BF16),
+                                                (4, 0, F16, BF16), (8, 64, BF16, F16),
+                                                (8, 0, F16, F16)])
+def test_embed_gather_matches_library_rounding(oracle_mod, bits, group, sdt, odt):
+    rng = np.random.default_rng(bits + group + 3 * sdt + odt)
+    n, k = 37, 256
+    g = k if group == 0 else group
+    if bits == 4:
+        q = rng.integers(-8, 8, (n, k)).astype(np.int8)
+        qw = oracle.pack_int4((q + 8).astype(np.uint8))
+    else:
+        q = rng.integers(-127, 128, (n, k)).astype(np.int8)
+        qw = q
+    s32 = (rng.standard_normal((n, k // g)) * 0.05).astype(np.float32)
+    sbits = _f16_bits(s32) if sdt == F16 else _bf16_bits(s32)
+    sval = (sbits.view(np.float16).astype(np.float64) if sdt == F16 else
+            torch.tensor(sbits.view(np.int16)).view(torch.bfloat16).double().numpy())
+    ids = np.array([0, 36, 5, 5, -1, 37, 1000, 12], dtype=np.int32)
+    out = oracle.embed_gather(ids, qw, bits, sbits, sdt, group, n, k, odt)
+    for i, r in enumerate(ids):
+        if 0 <= r < n:
+            exact = q[r].astype(np.float64) * np.repeat(sval[r], g)    # exact in fp32 too
+            want = _f16_bits(exact.astype(np.float32)) if odt == F16 else \
+                _bf16_bits(exact.astype(np.float32))
+            np.testing.assert_array_equal(out[i], want)
+        else:
+            assert not out[i].any()                                   # +0 rows
+
+
+def test_embed_gather_overflow_and_int8_extremes(oracle_mod):
+    q = np.array([[127, -127, 1, 0, 0, 0, 0, 0]], dtype=np.int8)
+    fmax = np.array([[0x7BFF]], dtype=np.uint16)                      # fp16 65504
+    out16 = oracle.embed_gather(np.array([0]), q, 8, fmax, F16, 8, 1, 8, F16)
+    assert out16[0, :3].tolist() == [0x7C00, 0xFC00, 0x7BFF]          # +inf, -inf, 65504
+    outbf = oracle.embed_gather(np.array([0]), q, 8, fmax, F16, 8, 1, 8, BF16)
+    np.testing.assert_array_equal(outbf[0, :3], _bf16_bits([127 * 65504.0, -127 * 65504.0,
+                                                            65504.0]))

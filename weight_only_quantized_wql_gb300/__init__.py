@@ -13,6 +13,7 @@ Functions
   wql_logits(x, qw, bias=None, topk=0, workspace=None, out=None)
                                                     -> (logits, topk_idx, topk_val)
   wql_topk_rescore(x, w_ref, topk_idx, topk_val, logits, bias=None)
+  wql_embed_gather(ids, qw, out_dtype=torch.float16, out=None) -> [*ids.shape, k]
   wql_status_string, wql_last_error, wql_launch_count
 """
 from __future__ import annotations
@@ -29,6 +30,7 @@ from . import _build
 __all__ = [
     "WQLError", "QuantizedWeight", "Workspace", "load", "wql_quantize", "wql_pack",
     "wql_unpack", "wql_workspace_size", "wql_logits", "wql_logits_noalloc", "wql_topk_rescore",
+    "wql_embed_gather",
     "wql_status_string", "wql_last_error", "wql_launch_count", "F32", "F16", "BF16",
     "CLIP_RTN", "CLIP_MSE", "MAX_TOPK", "NOALLOC_SCRATCH_BYTES",
 ]
@@ -98,6 +100,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wql_topk_rescore.restype = i32
         lib.wql_topk_rescore.argtypes = [vp, i32, i64, vp, i32, i64, i64, vp, i32, vp, vp, vp,
                                          vp]
+        lib.wql_embed_gather.restype = i32
+        lib.wql_embed_gather.argtypes = [vp, i64, ctypes.POINTER(_WqlWeight), i32, vp, vp]
         lib.wql_status_string.restype = ctypes.c_char_p
         lib.wql_status_string.argtypes = [i32]
         lib.wql_last_error.restype = ctypes.c_char_p
@@ -345,3 +349,22 @@ def wql_topk_rescore(x: torch.Tensor, w_ref: torch.Tensor, topk_idx: torch.Tenso
     _check("wql_topk_rescore", lib.wql_topk_rescore(
         _ptr(x2), _DTYPE_CODE[x.dtype], m, _ptr(w_ref), _DTYPE_CODE[w_ref.dtype], n, k,
         _ptr(bias), topk, _ptr(topk_idx), _ptr(topk_val), _ptr(logits), _stream(x.device)))
+
+
+def wql_embed_gather(ids: torch.Tensor, qw: QuantizedWeight, out_dtype=torch.float16,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """Dequantised rows of the tied head for token ids (see wql.h): returns
+    [*ids.shape, k] of out_dtype; ids outside [0, n) give rows of zeros."""
+    lib = load()
+    if ids.dtype != torch.int32:
+        raise ValueError("ids must be int32")
+    flat = ids.reshape(-1)
+    _cuda(flat, "ids")
+    t = flat.numel()
+    if out is None:
+        out = torch.empty((t, qw.k), dtype=out_dtype, device=ids.device)
+    _cuda(out, "out")
+    st = qw._struct()
+    _check("wql_embed_gather", lib.wql_embed_gather(
+        _ptr(flat), t, ctypes.byref(st), _DTYPE_CODE[out.dtype], _ptr(out), _stream(ids.device)))
+    return out.reshape(*ids.shape, qw.k)

@@ -267,6 +267,38 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   return WQL_OK;
 }
 
+wql_status wql_embed_gather(const int32_t* ids, int64_t t, const wql_weight* w,
+                            int32_t out_dtype, void* out, cudaStream_t stream) {
+  if (!w || t < 0 || w->n < 0 || w->k <= 0 || w->group < 0 || w->reserved != 0)
+    return WQL_EINVAL;
+  const int64_t n = w->n, k = w->k;
+  if (t > 0 && (!ids || !out)) return WQL_EINVAL;
+  if (t > 0 && n > 0 && (!w->qweight || !w->scales)) return WQL_EINVAL;
+  if (w->bits != 4 && w->bits != 8) return WQL_EUNSUPPORTED;
+  if (!half_dtype(out_dtype) || !half_dtype(w->scale_dtype)) return WQL_EUNSUPPORTED;
+  const int64_t g = w->group == 0 ? k : w->group;
+  if (k % 8 != 0 || g % 8 != 0 || k % g != 0) return WQL_EUNSUPPORTED;
+  if (n >= (int64_t(1) << 31) || t >= (int64_t(1) << 31) || k >= (int64_t(1) << 30))
+    return WQL_EUNSUPPORTED;
+  if (!aligned(ids, 4) || !aligned(w->qweight, 8) || !aligned(w->scales, 2) || !aligned(out, 16))
+    return WQL_EUNSUPPORTED;
+  if (t == 0) return WQL_OK;
+  EmbedArgs a{};
+  a.ids = ids;
+  a.t = (int)t;
+  a.qweight = w->qweight;
+  a.scales = static_cast<const uint16_t*>(w->scales);
+  a.bits = w->bits;
+  a.group_eff = (int)g;
+  a.scale_dtype = w->scale_dtype;
+  a.n = (int)n;
+  a.k = (int)k;
+  a.out_dtype = out_dtype;
+  a.out = out;
+  cudaError_t e = launch_embed_gather(a, stream);
+  return e == cudaSuccess ? WQL_OK : cuda_fail(e);
+}
+
 wql_status wql_topk_rescore(const void* x, int32_t x_dtype, int64_t m, const void* w_ref,
                             int32_t wref_dtype, int64_t n, int64_t k, const void* bias,
                             int32_t topk, int32_t* topk_idx, float* topk_val,
