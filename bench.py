@@ -350,17 +350,14 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
     assert wql.wql_launch_count() - n0 == R, "one launch per call expected"
     kern_us = time_graph(g_dom, reps=max(3, args.steps // 4))
 
-    # ---- reduce over ranks: max time ----
-    vals = torch.tensor([dev_s, sum(e2e_us) * 1e-6, t_wall], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
-    dev_s, e2e_s, t_wall = (float(v) for v in vals.tolist())
+    # ---- reduce over ranks: the slowest rank's times ----
+    dev_s, e2e_s, t_wall = aggregate_over_ranks([dev_s, sum(e2e_us) * 1e-6, t_wall], world,
+                                                device=dev)
     if rank != 0:
         return None
 
     pk = peaks()
-    total_bytes = step_bytes(MS) * args.steps * world
-    value = total_bytes / dev_s / 1e9
+    value = job_throughput_gbs(step_bytes(MS), args.steps, world, dev_s)
     med = {m: statistics.median(logit_us[m]) for m in MS}   # each entry: mean of R calls
     calls = {}
     for m in MS:
@@ -413,7 +410,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
         "calls": calls, "quantize_ms": round(quant_ms, 3),
         "roofline": roof,
         "cpu_baseline": None,
-        "e2e": {"value": round(step_bytes(MS) * args.steps * world / e2e_s / 1e9, 1),
+        "e2e": {"value": round(job_throughput_gbs(step_bytes(MS), args.steps, world, e2e_s), 1),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "wall_s_timed": round(t_wall, 4),
@@ -687,14 +684,21 @@ def run_reference(args) -> dict:
 
 # ---------------------------------------------------------------------------
 
-def aggregate_over_ranks(local: list[float], world: int, op: str = "max") -> list[float]:
-    """Reduce per-rank timings (max) across the process group."""
+def aggregate_over_ranks(local: list[float], world: int, device=None) -> list[float]:
+    """Every rank's timings reduced to the slowest rank's (MAX) across the
+    process group: a tensor on `device` (CUDA under NCCL, CPU under gloo)."""
     import torch
     import torch.distributed as dist
-    t = torch.tensor(local, dtype=torch.float64)
+    t = torch.tensor(local, dtype=torch.float64, device=device)
     if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
-    return t.tolist()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput_gbs(step_bytes_: int, steps: int, world: int, slowest_s: float) -> float:
+    """Whole-job GB/s: the bytes all replicas moved over the slowest rank's
+    time (each rank runs the same step on its own copy of the head)."""
+    return step_bytes_ * steps * world / slowest_s / 1e9
 
 
 def main(argv=None):

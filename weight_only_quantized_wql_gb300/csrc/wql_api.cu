@@ -14,6 +14,7 @@
 
 #include "sm100.cuh"
 #include "wql_common.cuh"
+#include "embed.cuh"
 
 namespace wql {
 
