@@ -23,6 +23,10 @@ it with numpy arrays.  Each wrapper names the page section it follows:
 * ``embed_gather`` -- same page, Purpose (tied head: a token's input
   embedding is that row of the dequantised weight), rounded once to
   fp16 / bf16.
+* ``e4m3_*``, ``quantize_fp8``, ``logits_fp8`` -- the per-channel fp8 head
+  that radiance_lmhead_int4.py's module docstring compares against: e4m3
+  from the format's definition, a per-row scale rounded before the codes
+  are chosen, binary64 logits.
 """
 from __future__ import annotations
 
@@ -88,6 +92,14 @@ def _load():
         lib.oracle_topk.argtypes = [vp, i64, i64, i32, vp, vp]
         lib.oracle_embed_gather.restype = i32
         lib.oracle_embed_gather.argtypes = [vp, i64, vp, i32, vp, i32, i64, i64, i64, i32, vp]
+        lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_f64_to_e4m3.restype = ctypes.c_uint8
+        lib.oracle_f64_to_e4m3.argtypes = [ctypes.c_double]
+        lib.oracle_quantize_fp8.restype = i32
+        lib.oracle_quantize_fp8.argtypes = [vp, i32, i64, i64, i32, vp, vp]
+        lib.oracle_logits_fp8.restype = i32
+        lib.oracle_logits_fp8.argtypes = [vp, i32, i64, i64, vp, vp, i32, i64, vp, vp]
         lib.oracle_rescore.restype = i32
         lib.oracle_rescore.argtypes = [vp, i32, i64, i64, vp, i32, i64, vp, i32, vp, i32, vp, vp]
         _lib = lib
@@ -262,6 +274,47 @@ def embed_gather(ids: np.ndarray, qweight: np.ndarray, bits: int, scales: np.nda
     if rc != 0:
         raise ValueError("oracle_embed_gather rejected its arguments")
     return out
+
+
+def e4m3_to_f64(bits) -> np.ndarray:
+    lib = _load()
+    b = np.asarray(bits, dtype=np.uint8).ravel()
+    return np.array([lib.oracle_e4m3_to_f64(int(v)) for v in b], dtype=np.float64)
+
+
+def f64_to_e4m3(values) -> np.ndarray:
+    """Round to e4m3 (ties to even), saturating at +-448; NaN -> 0x7F."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float64).ravel()
+    return np.array([lib.oracle_f64_to_e4m3(float(x)) for x in v], dtype=np.uint8)
+
+
+def quantize_fp8(w: np.ndarray, w_dtype: int, scale_dtype: int):
+    """(e4m3 codes uint8 [n, k], per-row scale bits uint16 [n])."""
+    lib = _load()
+    n, k = w.shape
+    wb = _as_bits(w, w_dtype)
+    q = np.empty((n, k), dtype=np.uint8)
+    s = np.empty(n, dtype=np.uint16)
+    if lib.oracle_quantize_fp8(_ptr(wb), w_dtype, n, k, scale_dtype, _ptr(q), _ptr(s)) != 0:
+        raise ValueError("oracle_quantize_fp8 rejected its arguments")
+    return q, s
+
+
+def logits_fp8(x: np.ndarray, x_dtype: int, q: np.ndarray, scales: np.ndarray,
+               scale_dtype: int):
+    """binary64 logits [m, n] of the fp8 head and the matching sum |x*w|."""
+    lib = _load()
+    xb = _as_bits(x, x_dtype)
+    m, k = xb.shape
+    qq = np.ascontiguousarray(q, dtype=np.uint8)
+    n = qq.shape[0]
+    sc = np.ascontiguousarray(scales).view(np.uint16)
+    out = np.empty((m, n), dtype=np.float64)
+    absout = np.empty((m, n), dtype=np.float64)
+    lib.oracle_logits_fp8(_ptr(xb), x_dtype, m, k, _ptr(qq), _ptr(sc), scale_dtype, n,
+                          _ptr(out), _ptr(absout))
+    return out, absout
 
 
 def tolerance(absacc: np.ndarray) -> np.ndarray:

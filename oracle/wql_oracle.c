@@ -500,3 +500,99 @@ int oracle_embed_gather(const int32_t* ids, int64_t t, const void* qweight, int 
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* fp8 e4m3 per-row head (the fp8 lm_head the radiance_lmhead_int4.py       */
+/* module docstring compares against: per-channel fp8).                     */
+/* e4m3 ("fn" variant): sign, 4 exponent bits with bias 7, 3 mantissa bits; */
+/* no infinities, the all-ones pattern is NaN, largest finite 448,          */
+/* subnormals m * 2^-9.  Readings (the page gives no formula): the row's    */
+/* scale is s = RN_sdtype(max(fl32(amax) *f32 fl32(1/448), 1e-8f)), rounded */
+/* before the codes are chosen, as for int4; q = RN_e4m3(clamp(w /f32 s,    */
+/* -448, 448)), ties to even; a zero scale gives q = 0.                      */
+/* ------------------------------------------------------------------------ */
+
+double oracle_e4m3_to_f64(uint8_t b) {
+  const int neg = (b >> 7) & 1;
+  const int e = (b >> 3) & 15;
+  const int m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m, -9);
+  else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return neg ? -v : v;
+}
+
+uint8_t oracle_f64_to_e4m3(double v) {
+  if (isnan(v)) return 0x7F;
+  const int neg = signbit(v) ? 1 : 0;
+  double a = fabs(v);
+  if (a > 448.0) a = 448.0;                         /* saturate */
+  /* 4 significant bits, minimum normal exponent -6: round_to_format handles
+     the subnormal quantum 2^-9; results stay <= 448 (448 is representable) */
+  const double r = round_to_format(a, 4, -6, 8);
+  uint8_t bits;
+  if (r == 0.0) {
+    bits = 0;
+  } else {
+    int e;
+    frexp(r, &e);
+    int ex = e - 1;
+    if (ex < -6) {
+      bits = (uint8_t)(r / ldexp(1.0, -9));         /* subnormal: m * 2^-9 */
+    } else {
+      const int mant = (int)((r / ldexp(1.0, ex) - 1.0) * 8.0);
+      bits = (uint8_t)(((ex + 7) << 3) | mant);
+    }
+  }
+  return (uint8_t)(bits | (neg << 7));
+}
+
+/* w: n*k values of w_dtype; q_out: n*k e4m3 bytes; scales_out: n storage-dtype bits. */
+int oracle_quantize_fp8(const void* w, int w_dtype, int64_t n, int64_t k, int scale_dtype,
+                        uint8_t* q_out, uint16_t* scales_out) {
+  if (k <= 0 || (scale_dtype != OR_F16 && scale_dtype != OR_BF16)) return -1;
+  const float inv = (float)(1.0 / 448.0);
+  for (int64_t r = 0; r < n; ++r) {
+    float amax = 0.0f;
+    for (int64_t kk = 0; kk < k; ++kk) {
+      const float a = fabsf((float)load_elem(w, w_dtype, r * k + kk));
+      if (a > amax) amax = a;
+    }
+    float s = amax * inv;
+    if (s < 1e-8f) s = 1e-8f;
+    const uint16_t sb = store_scale(s, scale_dtype);
+    scales_out[r] = sb;
+    const float sf = (float)scale_value(sb, scale_dtype);
+    for (int64_t kk = 0; kk < k; ++kk) {
+      if (sf == 0.0f) { q_out[r * k + kk] = 0; continue; }
+      float t = (float)load_elem(w, w_dtype, r * k + kk) / sf;
+      if (t > 448.0f) t = 448.0f;
+      if (t < -448.0f) t = -448.0f;
+      q_out[r * k + kk] = oracle_f64_to_e4m3((double)t);
+    }
+  }
+  return 0;
+}
+
+/* out[m, n] = sum_k x[m,k] * (e4m3(q[n,k]) * s[n]) in binary64, k ascending;
+ * abs_out (nullable) the matching sum |x * w|. */
+int oracle_logits_fp8(const void* x, int x_dtype, int64_t m, int64_t k, const uint8_t* q,
+                      const uint16_t* scales, int scale_dtype, int64_t n, double* out,
+                      double* abs_out) {
+  for (int64_t r = 0; r < n; ++r) {
+    const double s = scale_value(scales[r], scale_dtype);
+    for (int64_t mi = 0; mi < m; ++mi) {
+      double acc = 0.0, absacc = 0.0;
+      for (int64_t kk = 0; kk < k; ++kk) {
+        const double p = load_elem(x, x_dtype, mi * k + kk) *
+                         (oracle_e4m3_to_f64(q[r * k + kk]) * s);
+        acc = acc + p;
+        absacc = absacc + fabs(p);
+      }
+      out[mi * n + r] = acc;
+      if (abs_out) abs_out[mi * n + r] = absacc;
+    }
+  }
+  return 0;
+}

@@ -427,3 +427,84 @@ def test_embed_gather_overflow_and_int8_extremes(oracle_mod):
     outbf = oracle.embed_gather(np.array([0]), q, 8, fmax, F16, 8, 1, 8, BF16)
     np.testing.assert_array_equal(outbf[0, :3], _bf16_bits([127 * 65504.0, -127 * 65504.0,
                                                             65504.0]))
+
+
+# --------------------------------------------------------------------------
+# fp8 e4m3 per-row head
+# --------------------------------------------------------------------------
+
+def _torch_e4m3_decode(bits):
+    return torch.tensor(np.asarray(bits, dtype=np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def test_e4m3_decode_all_patterns(oracle_mod):
+    bits = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_to_f64(bits)
+    want = _torch_e4m3_decode(bits)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2       # 0x7F, 0xFF
+    np.testing.assert_array_equal(got[~nan], want[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_rounding(oracle_mod):
+    rng = np.random.default_rng(4)
+    finite = _torch_e4m3_decode(np.arange(256, dtype=np.uint8))
+    finite = np.unique(finite[~np.isnan(finite)])
+    mids = (finite[:-1] + finite[1:]) / 2                                 # exact ties
+    v = np.concatenate([finite, mids, -mids, rng.uniform(-448, 448, 4000),
+                        rng.uniform(-1, 1, 2000) * 2.0 ** rng.integers(-12, 2, 2000)])
+    v = v.astype(np.float32)                                              # one rounding each
+    v = v[np.abs(v) <= 448]
+    got = oracle.f64_to_e4m3(v.astype(np.float64))
+    want = torch.tensor(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(got, want)
+
+
+def test_e4m3_encode_saturates(oracle_mod):
+    # reading: beyond the largest finite value the code saturates at +-448
+    got = oracle.f64_to_e4m3([449.0, 480.0, 1e30, -465.0, -1e30])
+    assert got.tolist() == [0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+
+
+@pytest.mark.parametrize("sdt", [F16, BF16])
+def test_quantize_fp8_is_nearest_and_hits_the_range(oracle_mod, sdt):
+    rng = np.random.default_rng(sdt)
+    n, k = 6, 96
+    w = (rng.standard_normal((n, k)) * 0.02).astype(np.float32)
+    w[2] = 0.0                                                            # zero row
+    w[3, 7] = -0.5                                                        # outlier
+    q, s = oracle.quantize_fp8(w, F32, sdt)
+    sval = (s.view(np.float16).astype(np.float64) if sdt == F16 else
+            torch.tensor(s.view(np.int16)).view(torch.bfloat16).double().numpy())
+    finite = _torch_e4m3_decode(np.arange(256, dtype=np.uint8))
+    codes = [c for c in range(256) if not np.isnan(finite[c])]
+    for r in range(n):
+        if sval[r] == 0.0:
+            assert not q[r].any()
+            continue
+        amax_col = int(np.argmax(np.abs(w[r])))
+        if np.abs(w[r]).max() > 0:
+            assert abs(finite[q[r, amax_col]]) == 448.0                   # the row's amax
+        for c in range(k):
+            t = Fraction(float(np.float32(np.float32(w[r, c]) / np.float32(sval[r]))))
+            t = max(Fraction(-448), min(Fraction(448), t))
+            best = min(abs(Fraction(float(finite[cd])) - t) for cd in codes)
+            ties = [cd for cd in codes if abs(Fraction(float(finite[cd])) - t) == best]
+            chosen = int(q[r, c])
+            assert chosen in ties or (finite[chosen] == 0.0 and any(finite[cd] == 0.0 for cd in ties))
+            if len({float(finite[cd]) for cd in ties}) > 1:               # exact tie: even mantissa
+                assert chosen & 1 == 0
+
+
+def test_logits_fp8_match_dense_product(oracle_mod):
+    rng = np.random.default_rng(8)
+    n, k, m = 40, 128, 3
+    w = (rng.standard_normal((n, k)) * 0.02).astype(np.float32)
+    q, s = oracle.quantize_fp8(w, F32, F16)
+    x = rng.standard_normal((m, k)).astype(np.float16)
+    dense = _torch_e4m3_decode(q) * s.view(np.float16).astype(np.float64)[:, None]
+    want = x.astype(np.float64) @ dense.T
+    got, absacc = oracle.logits_fp8(x.view(np.uint16), F16, q, s, F16)
+    assert np.all(np.abs(got - want) <= 1e-12 * absacc + 1e-300)
+    np.testing.assert_allclose(absacc, np.abs(x.astype(np.float64)) @ np.abs(dense).T, rtol=1e-12)
