@@ -27,6 +27,9 @@ it with numpy arrays.  Each wrapper names the page section it follows:
   that radiance_lmhead_int4.py's module docstring compares against: e4m3
   from the format's definition, a per-row scale rounded before the codes
   are chosen, binary64 logits.
+* ``quantize_asym_int4`` / ``logits_asym_int4`` -- zero-point int4 ("[CORE]
+  Quantized lm-head Framework": the test model's lm_head uses sym=False):
+  plain asymmetric round-to-nearest per group, w ~ (q - z) * s.
 """
 from __future__ import annotations
 
@@ -100,6 +103,11 @@ def _load():
         lib.oracle_quantize_fp8.argtypes = [vp, i32, i64, i64, i32, vp, vp]
         lib.oracle_logits_fp8.restype = i32
         lib.oracle_logits_fp8.argtypes = [vp, i32, i64, i64, vp, vp, i32, i64, vp, vp]
+        lib.oracle_quantize_asym_int4.restype = i32
+        lib.oracle_quantize_asym_int4.argtypes = [vp, i32, i64, i64, i32, i32, vp, vp, vp]
+        lib.oracle_logits_asym_int4.restype = i32
+        lib.oracle_logits_asym_int4.argtypes = [vp, i32, i64, i64, vp, vp, vp, i32, i32, i64,
+                                                vp, vp]
         lib.oracle_rescore.restype = i32
         lib.oracle_rescore.argtypes = [vp, i32, i64, i64, vp, i32, i64, vp, i32, vp, i32, vp, vp]
         _lib = lib
@@ -314,6 +322,38 @@ def logits_fp8(x: np.ndarray, x_dtype: int, q: np.ndarray, scales: np.ndarray,
     absout = np.empty((m, n), dtype=np.float64)
     lib.oracle_logits_fp8(_ptr(xb), x_dtype, m, k, _ptr(qq), _ptr(sc), scale_dtype, n,
                           _ptr(out), _ptr(absout))
+    return out, absout
+
+
+def quantize_asym_int4(w: np.ndarray, w_dtype: int, group: int, scale_dtype: int):
+    """(codes uint8 [n, k] in 0..15, scale bits uint16 [n, k/G], zero points uint8 [n, k/G])."""
+    lib = _load()
+    n, k = w.shape
+    wb = _as_bits(w, w_dtype)
+    q = np.empty((n, k), dtype=np.uint8)
+    s = np.empty((n, k // group), dtype=np.uint16)
+    z = np.empty((n, k // group), dtype=np.uint8)
+    if lib.oracle_quantize_asym_int4(_ptr(wb), w_dtype, n, k, group, scale_dtype, _ptr(q),
+                                     _ptr(s), _ptr(z)) != 0:
+        raise ValueError("oracle_quantize_asym_int4 rejected its arguments")
+    return q, s, z
+
+
+def logits_asym_int4(x: np.ndarray, x_dtype: int, q: np.ndarray, scales: np.ndarray,
+                     zeros: np.ndarray, scale_dtype: int, group: int):
+    """binary64 logits [m, n] of the zero-point int4 head and the matching sum |x*w|."""
+    lib = _load()
+    xb = _as_bits(x, x_dtype)
+    m, k = xb.shape
+    qq = np.ascontiguousarray(q, dtype=np.uint8)
+    n = qq.shape[0]
+    sc = np.ascontiguousarray(scales).view(np.uint16)
+    zz = np.ascontiguousarray(zeros, dtype=np.uint8)
+    out = np.empty((m, n), dtype=np.float64)
+    absout = np.empty((m, n), dtype=np.float64)
+    if lib.oracle_logits_asym_int4(_ptr(xb), x_dtype, m, k, _ptr(qq), _ptr(sc), _ptr(zz),
+                                   scale_dtype, group, n, _ptr(out), _ptr(absout)) != 0:
+        raise ValueError("oracle_logits_asym_int4 rejected its arguments")
     return out, absout
 
 

@@ -596,3 +596,78 @@ int oracle_logits_fp8(const void* x, int x_dtype, int64_t m, int64_t k, const ui
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Zero-point (asymmetric) int4 ("[CORE] Quantized lm-head Framework": its  */
+/* test model's lm_head is quantised with sym=False).  The page gives no    */
+/* formula; the reading is plain asymmetric round-to-nearest per group:     */
+/*   s = RN_sdtype(max((fl32(max) -f32 fl32(min)) *f32 fl32(1/15), 1e-8f))   */
+/*   with min <= 0 <= max over the group (so 0 is representable),            */
+/*   z = clamp(rint_even(-min /f32 s), 0, 15)  (an integer zero point),     */
+/*   q = clamp(rint_even(w /f32 s) + z, 0, 15), w ~ (q - z) * s.            */
+/* A zero scale gives q = z = 0.  q_out: n*k codes 0..15; scales_out and    */
+/* zeros_out: n*(k/group).                                                   */
+/* ------------------------------------------------------------------------ */
+int oracle_quantize_asym_int4(const void* w, int w_dtype, int64_t n, int64_t k, int group,
+                              int scale_dtype, uint8_t* q_out, uint16_t* scales_out,
+                              uint8_t* zeros_out) {
+  if (group <= 0 || k % group != 0 || (scale_dtype != OR_F16 && scale_dtype != OR_BF16))
+    return -1;
+  const int64_t ng = k / group;
+  const float inv15 = (float)(1.0 / 15.0);
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t g = 0; g < ng; ++g) {
+      float lo = 0.0f, hi = 0.0f;
+      for (int64_t j = 0; j < group; ++j) {
+        const float v = (float)load_elem(w, w_dtype, r * k + g * group + j);
+        if (v < lo) lo = v;
+        if (v > hi) hi = v;
+      }
+      float s = (hi - lo) * inv15;
+      if (s < 1e-8f) s = 1e-8f;
+      const uint16_t sb = store_scale(s, scale_dtype);
+      scales_out[r * ng + g] = sb;
+      const float sf = (float)scale_value(sb, scale_dtype);
+      int z = 0;
+      if (sf != 0.0f) {
+        z = (int)rintf(-lo / sf);
+        if (z < 0) z = 0;
+        if (z > 15) z = 15;
+      }
+      zeros_out[r * ng + g] = (uint8_t)z;
+      for (int64_t j = 0; j < group; ++j) {
+        const int64_t i = r * k + g * group + j;
+        int q = 0;
+        if (sf != 0.0f) {
+          q = (int)rintf((float)load_elem(w, w_dtype, i) / sf) + z;
+          if (q < 0) q = 0;
+          if (q > 15) q = 15;
+        }
+        q_out[i] = (uint8_t)q;
+      }
+    }
+  return 0;
+}
+
+/* out[m, n] = sum_k x[m,k] * ((q[n,k] - z[n,g]) * s[n,g]) in binary64, k ascending. */
+int oracle_logits_asym_int4(const void* x, int x_dtype, int64_t m, int64_t k, const uint8_t* q,
+                            const uint16_t* scales, const uint8_t* zeros, int scale_dtype,
+                            int group, int64_t n, double* out, double* abs_out) {
+  if (group <= 0 || k % group != 0) return -1;
+  const int64_t ng = k / group;
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t mi = 0; mi < m; ++mi) {
+      double acc = 0.0, absacc = 0.0;
+      for (int64_t kk = 0; kk < k; ++kk) {
+        const int64_t gi = r * ng + kk / group;
+        const double wv = (double)((int)q[r * k + kk] - (int)zeros[gi]) *
+                          scale_value(scales[gi], scale_dtype);
+        const double p = load_elem(x, x_dtype, mi * k + kk) * wv;
+        acc = acc + p;
+        absacc = absacc + fabs(p);
+      }
+      out[mi * n + r] = acc;
+      if (abs_out) abs_out[mi * n + r] = absacc;
+    }
+  return 0;
+}

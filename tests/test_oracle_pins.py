@@ -508,3 +508,66 @@ def test_logits_fp8_match_dense_product(oracle_mod):
     got, absacc = oracle.logits_fp8(x.view(np.uint16), F16, q, s, F16)
     assert np.all(np.abs(got - want) <= 1e-12 * absacc + 1e-300)
     np.testing.assert_allclose(absacc, np.abs(x.astype(np.float64)) @ np.abs(dense).T, rtol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# zero-point (asymmetric) int4
+# --------------------------------------------------------------------------
+
+def test_asym_int4_worked_example(oracle_mod):
+    # min -0.3, max 0.45: s = RN_fp16(0.75 / 15) = 0x2A66 (0.049988...), z = rint(0.3 / s) = 6,
+    # q = rint(w / s) + 6: -0.3 -> 0, 0 -> 6, 0.2 -> 10, 0.45 -> 15, -0.1 -> 4, 0.05 -> 7,
+    # 0.3 -> 12, 0.15 -> 9 (worked by hand)
+    w = np.array([[-0.3, 0.0, 0.2, 0.45, -0.1, 0.05, 0.3, 0.15]], dtype=np.float32)
+    q, s, z = oracle.quantize_asym_int4(w, F32, 8, F16)
+    assert q[0].tolist() == [0, 6, 10, 15, 4, 7, 12, 9]
+    assert s[0, 0] == 0x2A66 and z[0, 0] == 6
+
+
+@pytest.mark.parametrize("sdt", [F16, BF16])
+def test_asym_int4_codes_are_nearest(oracle_mod, sdt):
+    rng = np.random.default_rng(10 + sdt)
+    n, k, g = 5, 128, 32
+    w = (rng.standard_normal((n, k)) * 0.02 + rng.uniform(-0.01, 0.01, (n, 1))).astype(np.float32)
+    w[1, :g] = 0.0                                        # zero group
+    w[2, g:2 * g] = np.abs(w[2, g:2 * g])                 # one-signed group: min is 0
+    q, s, z = oracle.quantize_asym_int4(w, F32, g, sdt)
+    sval = (s.view(np.float16).astype(np.float64) if sdt == F16 else
+            torch.tensor(s.view(np.int16)).view(torch.bfloat16).double().numpy())
+    assert q.max() <= 15 and z.max() <= 15
+    for r in range(n):
+        for c in range(k):
+            gi = c // g
+            if sval[r, gi] == 0.0:
+                assert q[r, c] == 0 and z[r, gi] == 0
+                continue
+            t = Fraction(float(np.float32(w[r, c]) / np.float32(sval[r, gi])))
+            zz = int(z[r, gi])
+            dist = {qq: abs(Fraction(qq - zz) - t) for qq in range(16)}
+            best = min(dist.values())
+            ties = [qq for qq, d in dist.items() if d == best]
+            assert int(q[r, c]) in ties
+            if len(ties) > 1:
+                assert (int(q[r, c]) - zz) % 2 == 0         # halfway: rint to even
+            if w[r, c] == 0.0:
+                assert q[r, c] == zz                      # zero is exact
+    # the group's zero point reproduces its minimum within half a step
+    for r in range(n):
+        for gi in range(k // g):
+            if sval[r, gi] == 0.0:
+                continue
+            lo = min(0.0, float(w[r, gi * g:(gi + 1) * g].min()))
+            assert abs(-int(z[r, gi]) * sval[r, gi] - lo) <= sval[r, gi] / 2 + 1e-12
+
+
+def test_asym_int4_logits_match_dense_product(oracle_mod):
+    rng = np.random.default_rng(12)
+    n, k, g, m = 30, 256, 64, 2
+    w = (rng.standard_normal((n, k)) * 0.02).astype(np.float32)
+    q, s, z = oracle.quantize_asym_int4(w, F32, g, F16)
+    x = rng.standard_normal((m, k)).astype(np.float16)
+    sv = np.repeat(s.view(np.float16).astype(np.float64), g, axis=1)
+    dense = (q.astype(np.float64) - np.repeat(z.astype(np.float64), g, axis=1)) * sv
+    want = x.astype(np.float64) @ dense.T
+    got, absacc = oracle.logits_asym_int4(x.view(np.uint16), F16, q, s, z, F16, g)
+    assert np.all(np.abs(got - want) <= 1e-12 * absacc + 1e-300)
