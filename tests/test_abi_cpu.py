@@ -133,3 +133,34 @@ def test_embed_gather_argument_checks(lib):
     assert call(_weight(), t=0) == OK                            # nothing launched
     assert call(_weight(), t=0, ids=None, out=None) == OK
     assert wql.wql_launch_count() == before
+
+
+def test_binding_refuses_host_tensors(lib):
+    """There is no CPU path: every entry point raises on host tensors before
+    any library call (nothing is launched, nothing falls back)."""
+    before = wql.wql_launch_count()
+    import torch
+    n, k = 64, 128
+    qw = wql.QuantizedWeight(torch.zeros(n, k // 8, dtype=torch.int32),
+                             torch.zeros(n, k // 64, dtype=torch.float16), 4, 64, n, k)
+    x = torch.zeros(2, k, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        wql.wql_quantize(torch.zeros(n, k), 4, 64)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        wql.wql_logits(x, qw, topk=0)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        wql.wql_embed_gather(torch.zeros(3, dtype=torch.int32), qw)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        wql.wql_topk_rescore(x, torch.zeros(n, k, dtype=torch.float16),
+                             torch.zeros(2, 8, dtype=torch.int32),
+                             torch.zeros(2, 8), torch.zeros(2, n, dtype=torch.float16))
+    assert wql.wql_launch_count() == before
+
+
+def test_missing_library_raises(monkeypatch):
+    """A missing libwql.so is an error, not a fallback."""
+    from weight_only_quantized_wql_gb300 import _build
+    monkeypatch.setattr(wql, "_lib", None)
+    monkeypatch.setattr(_build, "LIB", "/nonexistent/libwql.so")
+    with pytest.raises(RuntimeError, match="libwql.so not found"):
+        wql.load(build_if_missing=False)
