@@ -392,6 +392,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
                 "frac": round(achieved / pk["bf16_tflops"], 4), "traffic": traffic,
                 "kernel": kern, "call": f"M={dom_m}, top-K off", "launch_us": round(dom_us, 2),
                 "peak_note": f"{pk['source']} bf16 burst; fp16 dense rate is the same"}
+        if pk.get("bf16_tflops_sustained"):
+            roof["frac_of_sustained"] = round(achieved / pk["bf16_tflops_sustained"], 4)
     else:
         achieved = dom_bytes / (dom_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
