@@ -121,10 +121,10 @@ wql_status wql_unpack(const int32_t* packed, int64_t n, int64_t k,
                       uint8_t* nibbles_out, cudaStream_t stream);
 
 /* Bytes of workspace wql_logits needs for m token rows and top-K width topk
- * (n is the vocab size).  Pure host arithmetic; never touches the GPU.  The
- * buffer must be zero-filled once before its first use; every call leaves it
- * ready for the next.  Calls that may run concurrently need separate
- * workspaces. */
+ * (n is the vocab size; the need does not grow with it).  Pure host
+ * arithmetic; never touches the GPU.  The buffer must be zero-filled once
+ * before its first use; every call leaves it ready for the next.  Calls that
+ * may run concurrently need separate workspaces. */
 size_t wql_workspace_size(int64_t m, int64_t n, int32_t topk);
 
 /* Logits of a quantised lm_head ("Fused WNA16 GEMM for tied quantized lm_head
@@ -147,17 +147,17 @@ size_t wql_workspace_size(int64_t m, int64_t n, int32_t topk);
  *              group's scale).  The two can differ by the folding rounding
  *              (at most 2^-11 relative per weight).
  *   workspace  device, 256-byte aligned, ws_bytes >= wql_workspace_size(m, n,
- *              topk); may be NULL when topk == 0 (the decode kernel then
- *              splits the vocab rows evenly instead of handing work units
- *              out through the workspace's counter)
+ *              topk); may be NULL when topk == 0.  A workspace that is passed
+ *              is checked (size and alignment) whether or not topk is 0:
+ *              WQL_EWORKSPACE otherwise.
  * The kernel is chosen from m inside the library. */
 wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m,
                       const wql_weight* w, const void* bias, void* logits_out,
                       int32_t topk, int32_t* topk_idx, float* topk_val,
                       void* workspace, size_t ws_bytes, cudaStream_t stream);
 
-/* Size of the device scratch area that wql_logits_noalloc uses: 24 MiB. */
-#define WQL_NOALLOC_SCRATCH_BYTES ((size_t)24 << 20)
+/* Size of the device scratch area that wql_logits_noalloc uses: 4 MiB. */
+#define WQL_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 
 /* wql_logits without a workspace argument.  The pages have no counterpart:
  * this is an interface of this library for callers that cannot provide
@@ -166,24 +166,24 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m,
  * start-up.  Arguments, layouts and results are those of wql_logits, except:
  *   - Scratch is one fixed area of WQL_NOALLOC_SCRATCH_BYTES per device,
  *     inside the library (reserved by the CUDA runtime when it loads the
- *     library's code on the device).  The call allocates nothing.
- *   - Every token count runs the decode kernel, in slices of 16 token rows;
- *     a call whose slice needs more scratch than the area holds, i.e.
- *     wql_workspace_size(min(m, 16), n, topk) > WQL_NOALLOC_SCRATCH_BYTES
- *     (with top-K: about 64 * n + 1 MiB bytes at 16 rows and topk 8), is
- *     rejected with WQL_EWORKSPACE before anything is launched.
- *   - The first call on each device does a one-time setup (it looks up the
- *     area's device address with that device current); make that first call
- *     before any stream capture begins.  A failed setup returns WQL_ECUDA and
- *     is retried by the next call.
- *   - The area's first 256 bytes (ticket counter, error word, per-token
- *     top-K bounds and candidate counts) are cleared on `stream` at the
- *     start of every call (one small memset before the launches).
+ *     library's code on the device, and held until the process exits).  The
+ *     call allocates nothing.
+ *   - Every token count runs the decode kernel, in slices of at most 16
+ *     token rows.  A slice's scratch need, wql_workspace_size(rows, n, topk),
+ *     is at most about 2.1 MB whatever n is, so every valid call fits; a
+ *     call whose slice needed more than the area would be rejected with
+ *     WQL_EWORKSPACE before anything is launched.
+ *   - The first call on each device does a set-up (it looks up the area's
+ *     device address with that device current); it is done again after the
+ *     device's context has been replaced (cudaDeviceReset, for one).  Make
+ *     that first call before any stream capture begins.  A failed set-up
+ *     returns WQL_ECUDA and is retried by the next call.
+ *   - The area's first 256 bytes (the ticket counter of the top-K merge) are
+ *     cleared on `stream` at the start of every call (one small memset
+ *     before the launches).
  *   - Calls on one device share the area: calls that may be in flight at
  *     the same time (other streams, unsynchronised host threads) race and
- *     corrupt each other's outputs.  Serialise them.
- * An internal wait that timed out (a stalled GPU, never bad arguments) shows
- * as index -1 and NaN values in topk_idx / topk_val. */
+ *     corrupt each other's outputs.  Serialise them. */
 wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t m,
                               const wql_weight* w, const void* bias,
                               void* logits_out, int32_t topk,

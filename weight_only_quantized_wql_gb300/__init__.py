@@ -292,7 +292,7 @@ def wql_logits(x: torch.Tensor, qw: QuantizedWeight, bias: torch.Tensor | None =
     return logits, None, None
 
 
-NOALLOC_SCRATCH_BYTES = 24 << 20   # WQL_NOALLOC_SCRATCH_BYTES
+NOALLOC_SCRATCH_BYTES = 4 << 20    # WQL_NOALLOC_SCRATCH_BYTES
 
 
 def wql_logits_noalloc(x: torch.Tensor, qw: QuantizedWeight, bias: torch.Tensor | None = None,
@@ -325,8 +325,8 @@ def wql_logits_noalloc(x: torch.Tensor, qw: QuantizedWeight, bias: torch.Tensor 
     if status == 4:
         need = wql_workspace_size(min(m, 16), qw.n, topk)
         raise WQLError("wql_logits_noalloc", status,
-                       f"needs {need} bytes of scratch for 16-row slices of a {qw.n}-row "
-                       f"vocab with top-{topk}; the fixed area holds {NOALLOC_SCRATCH_BYTES}")
+                       f"needs {need} bytes of scratch for 16-row slices with top-{topk}; "
+                       f"the fixed area holds {NOALLOC_SCRATCH_BYTES}")
     _check("wql_logits_noalloc", status)
     logits = out.reshape(*lead, qw.n)
     if topk > 0:

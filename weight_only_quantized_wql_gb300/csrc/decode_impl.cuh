@@ -1,44 +1,62 @@
-// decode_impl.cuh -- the decode kernel template (included by decode_f16.cu and
-// decode_bf16.cu, which instantiate it per activation dtype).
+// decode_impl.cuh -- the decode kernel template (instantiated per activation
+// and scale dtype by decode_x<x>_s<s>.cu).
 //
-// Logits of a weight-only quantised lm_head for small token
-// counts (m <= 16), the bandwidth-bound decode case ("Fused WNA16 GEMM for
-// tied quantized lm_head logits", Perf evals rows at M = 1; reviewer comment
-// item 1: at M = 1 only the bytes moved matter).
+// Logits of a weight-only quantised lm_head for small token counts (m <= 16),
+// the bandwidth-bound decode case ("Fused WNA16 GEMM for tied quantized
+// lm_head logits", Perf evals rows at M = 1; reviewer comment item 1: at
+// M = 1 only the bytes moved matter).
 //
-// Design (sm_103a, one persistent CTA per SM):
-//  * Work comes in units of up to 16 16-row vocab tiles (256 rows).  A CTA
-//    starts with the unit of its own index and takes further ones from a
-//    counter in the workspace, so CTAs whose copies stream faster take more
-//    (static strided units when there is no workspace).  Each unit streams
-//    along the hidden dimension in chunks of 128 packed bytes per row (256
-//    int4 or 128 int8 codes).
-//  * Warp 16 is the producer: one lane issues TMA tensor copies of every
-//    chunk (16-row boxes, 128B-swizzled) and, once per unit, a bulk copy of
-//    the unit's scale rows, into a 4-stage ring; each stage carries its unit
-//    id, and a last stage with id -1 tells the consumers to stop.  Activations are either
-//    resident in shared memory for the whole launch or, when m*k is too
-//    large for that, copied per chunk with the weights.
-//  * Warps 0..15 are consumers, one 16-row tile each.  ldmatrix moves packed
-//    words straight into the A-fragment layout of a warp MMA (m16n8k16, swap
-//    AB: vocab rows = M, tokens = N).  A code becomes the exact 16-bit value
-//    magic + u with one LOP3 (OffsetCodes); the MMA sums x*(q + offset) with
-//    exact products and fp32 accumulation, and offset * sum(x) -- computed
-//    once per launch for every (token, group) -- is subtracted per scale
-//    group before the exact fp32 scale multiply.
-//  * Top-K: the fp32 logits of the CTA's rows go to shared memory (or, when
-//    they do not fit, a global scratch row).  Each CTA takes a threshold per
-//    token -- the K-th largest of each warp's lane maxima, a lower bound of
-//    the K-th largest value -- keeps the rows at or above it and selects its
-//    top-K from those; it raises a per-token global bound with its K-th
-//    value and appends those of its K that reach the bound (as it stands
-//    after its own raise) to a per-token list in the workspace.  The last
-//    CTA to finish (atomic ticket, no waiting) ranks that short list: every
-//    entry of the final top-K reaches the final bound, hence the bound at
-//    its CTA's append, so it is on the list.
-//  * All mbarrier waits are bounded; a timeout sets the workspace error word
-//    and the CTA finishes without issuing further copies.
+// Design (sm_103a, one CTA per SM -- 16 warps, 8 when the MMAs take more than
+// one 8-column n-tile -- and no cross-warp handshakes on the streaming path):
+//  * The vocab is cut into 16-row tiles, split evenly over the CTAs (whole
+//    tiles).  Inside a CTA the tiles' "steps" -- 64 packed bytes of every row
+//    of a tile, i.e. 128 int4 or 64 int8 columns -- are split evenly over the
+//    warps in runs of kPD steps, so warps finish together even when a CTA
+//    holds only a few tiles per warp; a tile cut between two warps is summed
+//    through shared memory at the end.
+//  * Every warp streams its own rows: lane (g, t) copies 16 bytes of row g
+//    and of row g + 8 per step with cp.async (eight rows x 64 contiguous
+//    bytes per warp instruction) into its own slots of a per-warp ring of
+//    kPD steps, and later reads back exactly what it copied -- no handshake
+//    with any other lane or warp, no register ring.  Each step's copies go
+//    out as soon as the step kPD earlier has been consumed.
+//  * Codes become exact 16-bit values offset + u with one LOP3/PRMT
+//    (OffsetCodes), multiplied on the tensor cores by mma.sync m16n8k16
+//    (vocab rows = M, token columns = N, fp32 accumulation).  The offset
+//    times sum(x) over each step's columns is precomputed once per launch
+//    and enters the step's first MMA as its accumulator input (negated), so
+//    the chain sums exactly x*q; the scale of the step's group (every step
+//    lies in one group, or in one per 64-column half) then multiplies it in
+//    fp32.
+//  * The order of the hidden columns inside one MMA is free (x is permuted
+//    the same way), so a lane's 16 copied bytes feed its MMA fragments
+//    directly.  For int4 with 64-column groups a step spans two groups:
+//    lanes t = 0, 1 hold the first, t = 2, 3 the second.  Each group then
+//    gets its own MMA output column (column = 2 * token + group half, the B
+//    operand zero where the half does not match), which for m <= 4 costs no
+//    extra MMA.
+//  * x lives in shared memory for the whole launch (16-byte pieces XOR-
+//    swizzled by token), staged while the first weight copies are in flight;
+//    for fp16 int4 the columns read from the high nibble of each byte (the
+//    code times 16) are pre-scaled by 1/16, saving a shift per word.
+//  * Top-K: each warp keeps, per token, a short candidate buffer in shared
+//    memory and a threshold (the K-th largest value it has kept so far, a
+//    lower bound of the final K-th value).  A finished tile's values are
+//    compared against the threshold; the few that reach it are appended.  A
+//    buffer about to overflow is compacted to its K best, which raises the
+//    threshold.  At the end, per token, one warp takes the K best of the
+//    W buffers (K rounds of a warp maximum) and writes them, sorted, to the
+//    CTA's slot of the workspace.  The last CTA to take the ticket (acquire-
+//    release atomic) reads every slot's first entry; only the slots holding
+//    the K largest first entries can hold any of the final K, so it reads
+//    those K slots and takes the K best of their K x K entries.
+//  * Programmatic dependent launch: the kernel lets the next kernel on the
+//    stream launch early and reads x, the workspace and the outputs only
+//    after griddepcontrol.wait.  With static weights (LogitsArgs::
+//    weights_static) the first run's weight copies go out before the wait.
 #pragma once
+
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -49,846 +67,921 @@
 namespace wql {
 namespace decode_detail {
 
-constexpr int kConsumers = 16;
-constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kWarpsAll = kThreads / 32;
-constexpr int kBlockTiles = kConsumers;          // 16-row tiles per block
-constexpr int kChunkRowBytes = 128;              // packed bytes per row per chunk
-constexpr int kTileBytes = 16 * kChunkRowBytes;  // one TMA box
-constexpr int kStageWBytes = kBlockTiles * kTileBytes;
-constexpr int kStages = 4;
+constexpr int kMaxWarps = 16;
+constexpr int kPD = 4;             // steps per run = ring stages per warp
 constexpr int kMaxTok = 16;
-constexpr int kConsumerBarrier = 1;              // named barrier for the consumer warps
-constexpr int kSelCap = 256;                     // candidate slots per token in the selection
-constexpr int kTauWord = 16;                     // workspace word of token 0's global bound
-constexpr int kNCandWord = 32;                   // workspace word of token 0's candidate count
+constexpr int kZeroBytes = 1024;   // zero x region: a run of kPD steps of 16-byte pieces
+constexpr int kRingBytes = kPD * 2 * 32 * 16;   // per warp: kPD steps x rows g, g+8 x lanes
+
+// Warps per CTA of a variant: 16 for one n-tile, 8 for more (the wider
+// accumulators need more registers and x for 16 tokens more shared memory).
+__host__ __device__ constexpr int warps_of(int nt) { return nt == 1 ? 16 : 8; }
 
 struct DecodeParams {
   LogitsArgs a;
-  int tiles_total;      // ceil(n / 16)
-  int unit_tiles;       // 16-row tiles per work unit (a power of two <= kBlockTiles)
-  int unit_rows_log2;   // log2(16 * unit_tiles)
-  int units_total;      // ceil(tiles_total / unit_tiles)
-  int cap_units;        // most units one CTA takes (cap_units * grid >= units_total)
-  unsigned int* sched;  // [0] next unit - grid, [1] CTAs done; null: static units
-  uint32_t off_blk;     // int unit id per ring stage, then the CTA's unit ids in order
-  int chunks;           // chunks per row
-  int gunits;           // 64-column units per scale group
-  int ngroups;          // scale groups per row
-  int x_resident;       // 1: activations staged once; 0: per chunk by TMA
-  int xbox_bytes;       // per-chunk mode: bytes between activation boxes
-  uint32_t off_x, off_s, off_corr, off_bar, off_red;
-  int sbuf_bytes, nsb;  // scale buffer size and count
-  int scales_aligned;   // scale table 16-byte aligned (bulk copies allowed)
-  uint32_t off_vals;    // fp32 logits of the CTA's rows for the top-K, [token][vals_stride]
-  int vals_stride;      // 0: no room in shared memory, the global scratch row is used
-  unsigned int* err;    // sticky error word in the workspace (null: none)
+  int tiles;         // ceil(n / 16)
+  int tpc, tex;      // tiles per CTA: tpc, one more for the first tex CTAs
+  int rpt;           // runs (of kPD steps) per tile
+  int S;             // steps per tile, padded to a multiple of kPD
+  int S_real;        // steps holding packed columns: ceil(row_bytes / 64)
+  int group;         // columns per scale group
+  int ngroups;       // scale groups per row
+  int nunits;        // 64-column units of a (step-padded) row: 2 * S_real (int4) or S_real
+  int row_bytes;     // packed bytes per row
+  int corr_pitch;    // floats per corr line
+  int cap;           // candidate buffer entries per (warp, token): K + 16 to 32
+  uint32_t xpitch;   // bytes per token row of x in shared memory
+  uint32_t off_x, off_zero, off_corr, off_ring, off_list, off_cnt, off_misc, off_ugrp;
+  int early_weights;  // 1: weights may be read before the preceding kernel ends
 };
-
-// Working area of the top-K selection.  It lives in the weight ring, which is
-// free once the main loop has consumed every stage.
-struct SelWork {
-  unsigned int thr[kMaxTok];                   // value-key threshold per token
-  unsigned int cnt[kMaxTok];                   // entries kept per token
-  unsigned long long cand[kMaxTok][kSelCap];   // the kept keys
-};
-static_assert(sizeof(SelWork) <= (size_t)kStages * kStageWBytes, "selection area > ring");
 
 __host__ __device__ constexpr uint32_t round_up_u32(uint32_t v, uint32_t a) {
   return (v + a - 1) / a * a;
 }
 
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrier), "n"(kConsumers * 32) : "memory");
+// 16-byte async copy global -> shared, bypassing L1; src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Top-K keys of entries [0, count) per token, by all warps of the CTA: warp w
-// takes token w % m and every S-th stretch of 32 entries (S = warps / m);
-// loads go out in batches of 8 so L2 latency is paid once per batch.  Warps
-// w < m return their token's merged list in `out` (out_tok = w), others -1.
-template <int KT, typename Load>
-__device__ __forceinline__ void select_topk(int m, int K, int count, unsigned long long* red,
-                                            Load load, unsigned long long (&out)[KT],
-                                            int& out_tok) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int slices = max(1, kWarpsAll / m);
-  unsigned long long list[KT];
+// Scale entries are read through L1 (a row's scales serve several steps).
+__device__ __forceinline__ uint32_t ldg_scale(const uint16_t* p) {
+  uint16_t v;
+  asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return (uint32_t)v;
+}
+__device__ __forceinline__ uint32_t ldg_scale2(const uint16_t* p) {
+  uint32_t v;
+  asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Code conversion per variant: fp16 int4 reads the high nibble of each byte
+// in place (x pre-scaled by 1/16 there); everything else uses OffsetCodes.
+template <int BITS, typename XT>
+struct CodesOf {
+  using type = OffsetCodes<BITS, XT>;
+  static constexpr bool kScaledX = false;
+};
+template <>
+struct CodesOf<4, __half> {
+  using type = Int4F16Scaled;
+  static constexpr bool kScaledX = true;
+};
+
+// The value the MMA adds per code on top of x*q, per activation element:
+// the offset sum of one 16-byte piece of x as stored in shared memory.
+template <int BITS, typename XT>
+__device__ __forceinline__ float offset_sum(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float lo = 0.f, hi = 0.f;
 #pragma unroll
-  for (int i = 0; i < KT; ++i) list[i] = kEmptyKey;
-  if (warp < slices * m) {
-    const int tok = warp % m, sl = warp / m;
-    const int step = slices * 32;
-    for (int i0 = sl * 32 + lane; i0 < count; i0 += 8 * step) {
-      unsigned long long v[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int i = i0 + b * step;
-        v[b] = i < count ? load(tok, i) : kEmptyKey;
-      }
-#pragma unroll
-      for (int b = 0; b < 8; ++b) list_insert<KT>(list, v[b]);
-    }
+  for (int q = 0; q < 4; ++q) {
+    const float e0 = scale_bits_to_f32<XT>((uint16_t)(w[q] & 0xFFFFu));
+    const float e1 = scale_bits_to_f32<XT>((uint16_t)(w[q] >> 16));
+    if (CodesOf<BITS, XT>::kScaledX && (q & 1)) hi += e0 + e1;
+    else lo += e0 + e1;
   }
-  unsigned long long best[KT];
-  warp_merge_topk_redux<KT>(list, K, best);
-  if (warp < slices * m && lane < KT) red[warp * KT + lane] = pick(best, lane);
-  __syncthreads();
-  out_tok = -1;
-  if (warp < m) {
-    unsigned long long l2[KT];
-#pragma unroll
-    for (int i = 0; i < KT; ++i)
-      l2[i] = lane < slices ? red[(lane * m + warp) * KT + i] : kEmptyKey;
-    warp_merge_topk_redux<KT>(l2, K, out);
-    out_tok = warp;
+  if constexpr (CodesOf<BITS, XT>::kScaledX) return 1032.0f * lo + 1152.0f * hi;
+  else return OffsetCodes<BITS, XT>::kOffset * lo;
+}
+
+// Swizzle of x's 16-byte pieces inside each aligned run of 8 (by token).
+template <bool GW2>
+__device__ __forceinline__ uint32_t x_swz(int tok) {
+  return GW2 ? (uint32_t)(tok & 3) : (uint32_t)(tok & 7);
+}
+
+// m16n8k16 MMAs: accumulating in place (read-write accumulator operands, so
+// no copies surround a chain), and the chain's first one with a separate
+// accumulator input.
+template <typename XT> struct MmaOp;
+template <> struct MmaOp<__half> {
+  static __device__ __forceinline__ void acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
-}
+  static __device__ __forceinline__ void first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1, float c0, float c1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%10,%11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+  }
+};
+template <> struct MmaOp<__nv_bfloat16> {
+  static __device__ __forceinline__ void acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                             uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+  static __device__ __forceinline__ void first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1, float c0, float c1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%10,%11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+  }
+};
 
-__device__ __forceinline__ unsigned long long shfl_u64(unsigned long long v, int src) {
-  const uint32_t lo = __shfl_sync(0xFFFFFFFFu, (uint32_t)v, src);
-  const uint32_t hi = __shfl_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), src);
-  return ((unsigned long long)hi << 32) | lo;
-}
-
-// Order-preserving 32-bit key of a value (the high half of topk_key): NaN 0.
+// Order-preserving 32-bit key of a value (the high half of topk_key).
 __device__ __forceinline__ uint32_t value_key(float v) {
   if (v != v) return 0u;
   const uint32_t b = __float_as_uint(v + 0.0f);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// The K-th largest of the 32 lanes' values (K <= 32), on every lane: each
-// lane ranks its value against all others (ties by lane), 32 independent
-// shuffles, and the lane of rank K-1 broadcasts it.
-__device__ __forceinline__ uint32_t warp_kth_rank(uint32_t v, int K) {
-  const int lane = threadIdx.x & 31;
-  int rank = 0;
+// Rank (0 = largest) of `key` among the c keys at s (shared memory, 16-byte
+// aligned, keys unique): how many are larger.  Every lane reads the same
+// addresses (broadcasts), which costs far less than shuffling keys around
+// the warp.
+__device__ __forceinline__ int rank_smem(const unsigned long long* s, int c,
+                                         unsigned long long key) {
+  int r = 0;
+  // eight 16-byte loads in flight before any compare (each is a broadcast)
+  for (int j0 = 0; j0 < c; j0 += 16) {
+    ulonglong2 v[8];
 #pragma unroll
-  for (int j0 = 0; j0 < 32; j0 += 8) {
-    uint32_t o[8];   // eight shuffles in flight before any is used
+    for (int b = 0; b < 8; ++b)
+      v[b] = j0 + 2 * b < c ? *reinterpret_cast<const ulonglong2*>(s + j0 + 2 * b)
+                            : make_ulonglong2(0ull, 0ull);
 #pragma unroll
-    for (int b = 0; b < 8; ++b) o[b] = __shfl_sync(0xFFFFFFFFu, v, j0 + b);
-#pragma unroll
-    for (int b = 0; b < 8; ++b) rank += (o[b] > v || (o[b] == v && j0 + b < lane)) ? 1 : 0;
-  }
-  const unsigned int sel = __ballot_sync(0xFFFFFFFFu, rank == K - 1);
-  return __shfl_sync(0xFFFFFFFFu, v, __ffs(sel) - 1);
-}
-
-// Output of a warp's selection, per lane: the key for slot `slot` of the
-// descending top-K list (slot -1: this lane writes nothing).  Every slot
-// 0..K-1 is written by exactly one lane; kEmptyKey where there are fewer
-// than K entries.
-struct LaneSlot {
-  unsigned long long key;
-  int slot;
-};
-
-// Top K of c <= 32 unique keys held one per lane (lanes >= c: kEmptyKey):
-// each lane ranks its key by 32 shuffles and keeps slot = rank if rank < K.
-__device__ __forceinline__ LaneSlot warp_rank_of_32(unsigned long long key, int c, int K) {
-  const int lane = threadIdx.x & 31;
-  int rank = 0;
-#pragma unroll
-  for (int j0 = 0; j0 < 32; j0 += 8) {
-    unsigned long long o[8];   // eight shuffles in flight before any is used
-#pragma unroll
-    for (int b = 0; b < 8; ++b) o[b] = __shfl_sync(0xFFFFFFFFu, key, j0 + b);
-#pragma unroll
-    for (int b = 0; b < 8; ++b) rank += o[b] > key ? 1 : 0;
-  }
-  LaneSlot r{kEmptyKey, -1};
-  if (lane < c) {
-    if (rank < K) r = {key, rank};
-  } else if (lane < K) {
-    r = {kEmptyKey, lane};   // fewer than K entries: the empty tail slots
+    for (int b = 0; b < 8; ++b) {
+      const int j = j0 + 2 * b;
+      r += (j < c && v[b].x > key ? 1 : 0) + (j + 1 < c && v[b].y > key ? 1 : 0);
+    }
   }
   return r;
 }
 
-// The same output from a descending list held identically by every lane.
-template <int KT>
-__device__ __forceinline__ LaneSlot lane_slot_of_list(const unsigned long long (&out)[KT], int K) {
+// The K best of `count` keys load(i), by one warp (each lane a register
+// list, then the lanes merged); returned on every lane in `out`.
+template <int KT, typename Load>
+__device__ __forceinline__ void warp_topk_of(int count, int K, Load load,
+                                             unsigned long long (&out)[KT]) {
   const int lane = threadIdx.x & 31;
-  return lane < K ? LaneSlot{pick(out, lane), lane} : LaneSlot{kEmptyKey, -1};
+  unsigned long long list[KT];
+#pragma unroll
+  for (int i = 0; i < KT; ++i) list[i] = kEmptyKey;
+  for (int i0 = lane; i0 < count; i0 += 4 * 32) {
+    unsigned long long v[4];   // four loads in flight per lane
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int i = i0 + b * 32;
+      v[b] = i < count ? load(i) : kEmptyKey;
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) list_insert<KT>(list, v[b]);
+  }
+  warp_merge_topk_redux<KT>(list, K, out);
 }
 
-// Threshold selection of the top-K keys of entries [0, count) per token, by
-// all threads of the CTA.  vkey(t, i) reads entry i's value key (a 32-bit
-// key that orders values; 0 for NaN), fkey(t, i) its full 64-bit key (value
-// key high, index low).  W.thr[t] must hold a lower bound of token t's K-th
-// largest value key (0 if none) and W.cnt[t] zero, visible to all threads.
-// Each token's entries are spread over up to kSelWarps warps; every warp
-// raises the bound to the K-th largest of its lanes' maxima (K lanes hold
-// disjoint entries at or above it, so it does not exceed the token's K-th
-// largest value).  The entries whose value key reaches the bound are kept
-// (all of the top K are among them) and warp w < m selects token w's top K
-// from those (out_tok = w, slots in `res`; others -1).  Returns false, with
-// nothing selected, if a token kept more than kSelCap entries (many equal
-// values); the caller then selects exhaustively.
-constexpr int kSelWarps = 4;
-template <int KT, typename VKey, typename FKey>
-__device__ __forceinline__ bool cta_topk(int m, int K, int count, VKey vkey, FKey fkey,
-                                         SelWork& W, LaneSlot& res, int& out_tok) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int slices = max(1, min(kSelWarps, kWarpsAll / m));
-  const bool worker = warp < slices * m;
-  const int tok = warp % m, sl = warp / m;
-  const int step = slices * 32;
-  if (worker) {
-    uint32_t mx = 0u;
-    for (int i0 = sl * 32 + lane; i0 < count; i0 += 8 * step) {
-      uint32_t v[8];
+// The K best of keys spread over a warp, E per lane (unique but for
+// kEmptyKey), by K rounds of a warp-wide maximum (two hardware reductions:
+// value half, then index half among the lanes holding that value); the
+// lane holding a round's winner removes it.  The r-th best ends on lane r.
+template <int E>
+__device__ __forceinline__ unsigned long long warp_tournament(unsigned long long (&e)[E], int K) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long best = e[0];
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int i = i0 + b * step;
-        v[b] = vkey(tok, min(i, count - 1));
-        if (i >= count) v[b] = 0u;
-      }
+  for (int i = 1; i < E; ++i) best = e[i] > best ? e[i] : best;
+  unsigned long long mine = kEmptyKey;
+  for (int r = 0; r < K; ++r) {
+    const uint32_t hi = (uint32_t)(best >> 32);
+    const uint32_t mh = redux_max_u32(hi);
+    const uint32_t ml = redux_max_u32(hi == mh ? (uint32_t)best : 0u);
+    const unsigned long long top = ((unsigned long long)mh << 32) | ml;
+    if (lane == r) mine = top;
+    if (best == top && top != kEmptyKey) {
+      best = kEmptyKey;
 #pragma unroll
-      for (int b = 0; b < 8; ++b) mx = max(mx, v[b]);
-    }
-    const uint32_t kth = warp_kth_rank(mx, K);
-    if (lane == 0 && kth > 0u) atomicMax(&W.thr[tok], kth);
-  }
-  __syncthreads();
-  if (worker) {
-    const uint32_t th = W.thr[tok];
-    // warp-uniform trip count (the ballots below need every lane)
-    for (int w0 = sl * 32; w0 < count; w0 += 8 * step) {
-      const int i0 = w0 + lane;
-      uint32_t v[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int i = i0 + b * step;
-        v[b] = vkey(tok, min(i, count - 1));
-      }
-      // one shared atomic per warp for the batch's passing entries
-      unsigned int mask[8];
-      int total = 0;
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        mask[b] = __ballot_sync(0xFFFFFFFFu, i0 + b * step < count && v[b] >= th);
-        total += __popc(mask[b]);
-      }
-      if (total > 0) {
-        unsigned int at = 0u;
-        if (lane == 0) at = atomicAdd(&W.cnt[tok], (unsigned int)total);
-        at = __shfl_sync(0xFFFFFFFFu, at, 0);
-        const unsigned int lt = (1u << lane) - 1u;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          if (mask[b] >> lane & 1u) {
-            const unsigned int pos = at + __popc(mask[b] & lt);
-            if (pos < (unsigned int)kSelCap) W.cand[tok][pos] = fkey(tok, i0 + b * step);
-          }
-          at += __popc(mask[b]);
-        }
+      for (int i = 0; i < E; ++i) {
+        if (e[i] == top) e[i] = kEmptyKey;
+        best = e[i] > best ? e[i] : best;
       }
     }
   }
-  __syncthreads();
-  bool overflow = false;
-  for (int t = 0; t < m; ++t) overflow |= W.cnt[t] > (unsigned int)kSelCap;
-  out_tok = -1;
-  if (overflow) return false;
-  if (warp < m) {
-    const int c = (int)W.cnt[warp];
-    if (c <= 32) {
-      res = warp_rank_of_32(lane < c ? W.cand[warp][lane] : kEmptyKey, c, K);
-    } else {
-      unsigned long long list[KT], out[KT];
-#pragma unroll
-      for (int i = 0; i < KT; ++i) list[i] = kEmptyKey;
-      for (int i = lane; i < c; i += 32) list_insert<KT>(list, W.cand[warp][i]);
-      warp_merge_topk_redux<KT>(list, K, out);
-      res = lane_slot_of_list<KT>(out, K);
-    }
-    out_tok = warp;
-  }
-  return true;
+  return mine;
 }
 
 // Ticket of the last-CTA merge: an atomic add whose release makes this CTA's
-// candidate writes (ordered before it by the preceding block barrier)
-// visible before the ticket, and whose acquire, for the last CTA, makes the
-// other CTAs' candidates visible after it.
+// slot writes and threshold update (ordered before it by the preceding block
+// barrier) visible before the ticket, and whose acquire, for the last CTA,
+// makes the other CTAs' writes visible after it.
 __device__ __forceinline__ unsigned int ticket_add(unsigned int* t) {
   unsigned int old;
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
   return old;
 }
 
-// This CTA's candidates, the ticket, and (last CTA only) the final merge.
-// The CTA's rows are its nunits work units in the order it took them (unit
-// ids in blk_list, 2^rlog rows each; the grid's last unit, cut at n, is
-// always a CTA's last).  svals: their fp32 logits in shared memory
-// ([token][vals_stride], entry li * R + r), or null for the global scratch
-// row.
-template <int KT, typename XT, bool kSmemVals>
-__device__ __noinline__ void topk_tail(const DecodeParams& p, SelWork& W,
-                                          unsigned long long* red, unsigned int* flags,
-                                          int nunits, const int* blk_list, bool cta_bad,
-                                          const float* svals) {
-  const LogitsArgs& a = p.a;
-  unsigned int* err = p.err;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int m = a.m, n = a.n, K = a.topk;
-  unsigned int* tau = a.counter + kTauWord;   // per-token bound on the K-th value key
-  if (!cta_bad) {
-    const int rlog = p.unit_rows_log2, R = 1 << rlog;
-    const int count = nunits > 0 ? (nunits - 1) * R + min(R, n - blk_list[nunits - 1] * R) : 0;
-    const int vs = p.vals_stride;
-    auto rowof = [&](int i) { return blk_list[i >> rlog] * R + (i & (R - 1)); };
-    auto value = [&](int tk, int i) -> float {
-      if constexpr (kSmemVals) return svals[tk * vs + i];
-      else return __ldcg(a.scratch + (size_t)tk * n + rowof(i));
-    };
-    auto vkey = [&](int tk, int i) { return value_key(value(tk, i)); };
-    auto key = [&](int tk, int i) { return topk_key(value(tk, i), (uint32_t)rowof(i)); };
-    if (threadIdx.x < m) {
-      W.thr[threadIdx.x] = 0u;
-      W.cnt[threadIdx.x] = 0u;
-    }
-    __syncthreads();
-    LaneSlot res{kEmptyKey, -1};
-    int tok;
-    if (!cta_topk<KT>(m, K, count, vkey, key, W, res, tok)) {
-      unsigned long long best[KT];
-      select_topk<KT>(m, K, count, red, key, best, tok);
-      res = lane_slot_of_list<KT>(best, K);
-    }
-    if (tok >= 0) {
-      // every CTA's K-th value bounds the final K-th value from below: raise
-      // the token's bound, then append this CTA's entries that reach it as
-      // it stands after the raise (the reply of the atomic) -- an entry of
-      // the final top K reaches the final bound, hence this one, and the
-      // list stays short because later CTAs see an ever higher bound
-      const unsigned int kth_lane = __ballot_sync(0xFFFFFFFFu, res.slot == K - 1);
-      unsigned long long kth_key = shfl_u64(res.key, kth_lane ? __ffs(kth_lane) - 1 : 0);
-      if (kth_lane == 0u) kth_key = kEmptyKey;
-      uint32_t bound = 0u;
-      if (lane == 0 && kth_key != kEmptyKey)
-        bound = max(atomicMax(tau + tok, (uint32_t)(kth_key >> 32)), (uint32_t)(kth_key >> 32));
-      bound = __shfl_sync(0xFFFFFFFFu, bound, 0);
-      const bool pass = res.slot >= 0 && res.key != kEmptyKey && (uint32_t)(res.key >> 32) >= bound;
-      const unsigned int pm = __ballot_sync(0xFFFFFFFFu, pass);
-      unsigned int at = 0u;
-      if (lane == 0 && pm != 0u) at = atomicAdd(a.counter + kNCandWord + tok, (unsigned int)__popc(pm));
-      at = __shfl_sync(0xFFFFFFFFu, at, 0);
-      // at most K per CTA: the list never outgrows its WQL_MAX_CTAS * K slots
-      if (pass)
-        a.cand[(size_t)tok * WQL_MAX_CTAS * K + at + __popc(pm & ((1u << lane) - 1u))] = res.key;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) flags[1] = (ticket_add(a.counter) == gridDim.x - 1) ? 1u : 0u;
-  __syncthreads();
-  if (flags[1] == 0u) return;
-  // The error word (set by any CTA whose bounded wait timed out, before its
-  // ticket): with an error the results are replaced by "no entries".  A CTA
-  // that timed out itself reports no entries directly.
-  const unsigned int errv = __ldcg(err);
-  if (!cta_bad) {
-    // warp t ranks token t's appended candidates (m <= kMaxTok < warps)
-    if (warp < m) {
-      const unsigned long long* list = a.cand + (size_t)warp * WQL_MAX_CTAS * K;
-      // the first 32 slots are read together with the count (slots beyond
-      // it hold older entries and are masked): one round trip, not two
-      const unsigned long long first = __ldcg(list + lane);
-      const int c = (int)__ldcg(a.counter + kNCandWord + warp);
-      LaneSlot res{kEmptyKey, -1};
-      if (c <= 32) {
-        res = warp_rank_of_32(lane < c ? first : kEmptyKey, c, K);
-      } else {
-        unsigned long long best[KT], out[KT];
-#pragma unroll
-        for (int i = 0; i < KT; ++i) best[i] = kEmptyKey;
-        for (int i0 = lane; i0 < c; i0 += 8 * 32) {
-          unsigned long long v[8];   // eight loads in flight per lane
-#pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            const int i = i0 + 32 * b;
-            v[b] = i < c ? __ldcg(list + i) : kEmptyKey;
-          }
-#pragma unroll
-          for (int b = 0; b < 8; ++b) list_insert<KT>(best, v[b]);
-        }
-        warp_merge_topk_redux<KT>(best, K, out);
-        res = lane_slot_of_list<KT>(out, K);
-      }
-      if (res.slot >= 0) {
-        const bool ok = errv == 0u && res.key != kEmptyKey;
-        const size_t o = (size_t)warp * K + res.slot;
-        a.topk_idx[o] = ok ? key_index(res.key) : -1;
-        a.topk_val[o] = ok ? key_value(res.key) : __int_as_float(0x7FC00000);
-      }
-    }
-    __syncthreads();
-  } else {
-    // this CTA timed out: report no entries
-    for (int i = threadIdx.x; i < m * K; i += blockDim.x) {
-      a.topk_idx[i] = -1;
-      a.topk_val[i] = __int_as_float(0x7FC00000);
-    }
-  }
-  if (threadIdx.x == 0) *a.counter = 0u;       // ready for the next call
-  if (threadIdx.x < m) {
-    tau[threadIdx.x] = 0u;
-    a.counter[kNCandWord + threadIdx.x] = 0u;
-  }
-}
-
-// The offset sum of one 16-byte piece of 8 activations: off * sum(x); with
-// kScaled, the halves at elements 2, 3, 6, 7 hold x/16 and weigh 1152, the
-// others weigh 1032 (Int4F16Scaled).
-template <typename XT, bool kScaled>
-__device__ __forceinline__ float corr_piece(const uint4& v, float off) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float a = 0.f, b = 0.f;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float lo = scale_bits_to_f32<XT>((uint16_t)(w[q] & 0xFFFFu));
-    const float hi = scale_bits_to_f32<XT>((uint16_t)(w[q] >> 16));
-    if (kScaled && (q & 1)) b += lo + hi;
-    else a += lo + hi;
-  }
-  return kScaled ? 1032.0f * a + 1152.0f * b : off * a;
-}
-
-// tw:  packed weight, 16-row x 128-byte boxes (partial blocks)
-// twb: packed weight, 256-row x 128-byte boxes (one copy per full block chunk;
-//      TMA throughput is per box, so large boxes are what reach HBM speed)
-// tx:  activations, 64-column boxes of all m rows (per-chunk mode only)
-// Code conversion per variant: fp16 int4 with resident activations uses the
-// pre-scaled-activation form (one shift per word); everything else the
-// shifted OffsetCodes form.
-template <int BITS, typename XT, bool XRES>
-struct CodesFor {
-  using type = OffsetCodes<BITS, XT>;
-  static constexpr bool kScaledX = false;
-  static constexpr bool kCorr = OffsetCodes<BITS, XT>::kOffset != 0.0f;
-};
-template <>
-struct CodesFor<4, __half, true> {
-  using type = Int4F16Scaled;
-  static constexpr bool kScaledX = true;
-  static constexpr bool kCorr = true;
+// One warp's candidate buffers (shared memory): per token `cap` keys, their
+// count, and the threshold -- the value key of the K-th best kept so far
+// (0 until a compaction), below which no value can be among the final K.
+struct Cands {
+  unsigned long long* buf;   // [m][cap]
+  unsigned int* cnt;         // [m]
+  unsigned int* thr;         // [m]
+  int cap;
 };
 
-template <int BITS, typename XT, typename ST, int NT, bool XRES>
-__global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap twb,
-                  const __grid_constant__ CUtensorMap tx, const __grid_constant__ DecodeParams p) {
-  using CF = CodesFor<BITS, XT, XRES>;
-  using Codes = typename CF::type;
-  constexpr int kUnits = BITS == 4 ? 4 : 2;        // 64-column units per chunk
-  constexpr int KC = kUnits * 64;                  // codes per chunk
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;    // 1024-aligned for 128B swizzle
-  uint8_t* sm = smem_raw + (base - raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + p.off_bar);
-  uint64_t* empty = full + kStages;
-  unsigned int* flags = reinterpret_cast<unsigned int*>(empty + kStages);  // [0] bad, [1] last
-  unsigned long long* red = reinterpret_cast<unsigned long long*>(sm + p.off_red);
-  float* corr = reinterpret_cast<float*>(sm + p.off_corr);   // [kMaxTok][ngroups]
-  float* svals = reinterpret_cast<float*>(sm + p.off_vals);
-  int* blk_stage = reinterpret_cast<int*>(sm + p.off_blk);   // [kStages]
-  int* blk_list = blk_stage + kStages;                        // [cap_units]
-  const int U = p.unit_tiles;
-
-  const LogitsArgs& a = p.a;
+// Reduce token tk's buffer to its K best (one key per lane, cap <= 32), set
+// the count to min(count, K) and the threshold to the K-th best's value key
+// when there are K.  One shared copy of the code for every call site (kept
+// warm in the instruction cache by the compactions during the main loop).
+// (Arguments by value: a reference would put them in local memory.)
+static __device__ __noinline__ void compact_buf(unsigned long long* b, unsigned int* cnt,
+                                                unsigned int* thr, int cap, int K) {
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int m = a.m, n = a.n, k = a.k;
+  const int c = (int)min(*cnt, (unsigned int)cap);
+  const unsigned long long key = lane < c ? b[lane] : kEmptyKey;
+  const int rank = lane < c ? rank_smem(b, c, key) : 32;
+  __syncwarp();
+  if (rank < K) b[rank] = key;
+  if (lane == 0) *cnt = (unsigned int)min(c, K);
+  if (rank == K - 1) *thr = (uint32_t)(key >> 32);
+  __syncwarp();
+}
+__device__ __forceinline__ void compact(const Cands& C, int tk, int K) {
+  compact_buf(C.buf + tk * C.cap, C.cnt + tk, C.thr + tk, C.cap, K);
+}
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumers);
+// LIN: a step's scale entries are linear in the step -- with two group
+// halves, groups of 64 columns with the two halves' entries adjacent and
+// 4-byte aligned (one 32-bit load); otherwise one group per step.  Without
+// LIN they are looked up per step in a unit -> group table.
+template <int BITS, bool GW2, bool LIN, typename XT, typename ST, int NT>
+__global__ void __launch_bounds__(warps_of(NT) * 32, 1)
+    decode_kernel(const __grid_constant__ DecodeParams p) {
+  using Codes = typename CodesOf<BITS, XT>::type;
+  constexpr int W = warps_of(NT);
+  constexpr int kThr = W * 32;
+  constexpr bool kScaledX = CodesOf<BITS, XT>::kScaledX;
+  constexpr int kStepCols = BITS == 4 ? 128 : 64;       // columns per step
+  constexpr int kLanePieces = kStepCols / 32;           // 16-byte x pieces per lane per step
+  constexpr uint32_t kXStepBytes = kStepCols * 2;       // x bytes per step
+  constexpr bool kHasOffset = !(BITS == 8 && std::is_same<XT, __nv_bfloat16>::value);
+
+  extern __shared__ __align__(128) uint8_t sm[];
+  const LogitsArgs& a = p.a;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int m = a.m, n = a.n, k = a.k;
+  const int K = a.topk;
+
+  // ---- this CTA's tiles, this warp's runs of kPD steps ----
+  const int bid = (int)blockIdx.x;
+  const int T0 = bid * p.tpc + min(bid, p.tex);
+  const int T1 = T0 + p.tpc + (bid < p.tex ? 1 : 0);
+  const int rpt = p.rpt;                                    // runs per tile
+  const int nruns = (T1 - T0) * rpt;
+  const int rb = (int)((long long)nruns * warp / W);
+  const int re = (int)((long long)nruns * (warp + 1) / W);
+
+  const uint8_t* qw = reinterpret_cast<const uint8_t*>(a.qweight);
+  const uint16_t* scales = a.scales;
+  const int row_bytes = p.row_bytes;
+  const int ng = p.ngroups;
+  const uint32_t sm_base = smem_u32(sm);
+
+  // Scale group of each 64-column unit of a row (0xFFFF past k), for the
+  // layouts where a step's group is not a shift of its index.
+  uint16_t* ugrp = reinterpret_cast<uint16_t*>(sm + p.off_ugrp);
+  if (!LIN) {
+    for (int u = threadIdx.x; u < p.nunits; u += kThr)
+      ugrp[u] = u * 64 < k ? (uint16_t)((u * 64) / p.group) : (uint16_t)0xFFFF;
+    __syncthreads();
+  }
+
+  // ---- the weight ring: this warp's kPD stages, this lane's two 16-byte
+  //      slots per stage (rows g and g + 8) ----
+  const uint32_t ring = sm_base + p.off_ring + (uint32_t)warp * kRingBytes + (uint32_t)lane * 16u;
+  // stage j, row half h: ring + (2 * j + h) * 512
+
+  // A run's reading position: rows g and g + 8 of its tile (clamped to the
+  // last row; rows past n are never stored), its first step, how many of
+  // its steps hold columns.
+  struct RunPtr {
+    const uint8_t* pa;      // rows g / g + 8 at the run's first step and lane t's 16 bytes
+    const uint8_t* pb;
+    const uint16_t* spa;    // the rows' scale entries (at the run's first group when linear)
+    const uint16_t* spb;
+    int s0, nsteps;
+  };
+  auto run_ptr = [&](int tile, int r, bool live) {
+    RunPtr rp;
+    rp.s0 = r * kPD;
+    rp.nsteps = live ? min(kPD, p.S_real - rp.s0) : 0;
+    const int ra = min(tile * 16 + g, n - 1), rb8 = min(tile * 16 + g + 8, n - 1);
+    rp.pa = qw + (size_t)ra * row_bytes + rp.s0 * 64 + t * 16;
+    rp.pb = qw + (size_t)rb8 * row_bytes + rp.s0 * 64 + t * 16;
+    // scale entries: linear in the step (at the run's first one), or the
+    // rows' first entries for the table lookup
+    const int lin0 = LIN ? (GW2 ? 2 * rp.s0 : rp.s0) : 0;
+    rp.spa = scales + (size_t)ra * ng + lin0;
+    rp.spb = scales + (size_t)rb8 * ng + lin0;
+    return rp;
+  };
+  // The next run of the same tile: everything moves by one run.
+  auto run_next = [&](const RunPtr& c, bool live) {
+    RunPtr rp = c;
+    rp.s0 = c.s0 + kPD;
+    rp.nsteps = live ? min(kPD, p.S_real - rp.s0) : 0;
+    rp.pa = c.pa + kPD * 64;
+    rp.pb = c.pb + kPD * 64;
+    if (LIN) {
+      rp.spa = c.spa + (GW2 ? 2 * kPD : kPD);
+      rp.spb = c.spb + (GW2 ? 2 * kPD : kPD);
     }
-    flags[0] = 0u;
-    flags[1] = 0u;
-    fence_barrier_init();
+    return rp;
+  };
+  // Step j of a run: its weight copies into stage j (zeros past the row;
+  // nothing past the run's steps), as one commit group either way.
+  auto copy_step = [&](const RunPtr& rp, int j) {
+    if (j < rp.nsteps) {
+      const uint32_t src = (rp.s0 + j) * 64 + t * 16 < row_bytes ? 16u : 0u;
+      cp_async16(ring + (uint32_t)(2 * j) * 512u, rp.pa + j * 64, src);
+      cp_async16(ring + (uint32_t)(2 * j + 1) * 512u, rp.pb + j * 64, src);
+    }
+    cp_async_commit();
+  };
+  // The scales of step j of a run (rows g and g + 8).
+  auto load_scales = [&](const RunPtr& rp, int j, uint32_t& SA, uint32_t& SB) {
+    SA = 0u;
+    SB = 0u;
+    if (j < rp.nsteps) {
+      const int s = rp.s0 + j;
+      if constexpr (GW2 && LIN) {   // groups of 64: halves 2s and 2s + 1, adjacent
+        SA = ldg_scale2(rp.spa + 2 * j);
+        SB = ldg_scale2(rp.spb + 2 * j);
+      } else if constexpr (GW2) {
+        const int h0 = ugrp[2 * s], h1 = ugrp[2 * s + 1];
+        SA = ldg_scale(rp.spa + h0);
+        SB = ldg_scale(rp.spb + h0);
+        if (h1 != 0xFFFF) {
+          SA |= ldg_scale(rp.spa + h1) << 16;
+          SB |= ldg_scale(rp.spb + h1) << 16;
+        }
+      } else if constexpr (LIN) {   // one group per step
+        SA = ldg_scale(rp.spa + j);
+        SB = ldg_scale(rp.spb + j);
+      } else {
+        const int gi = ugrp[BITS == 4 ? 2 * s : s];
+        SA = ldg_scale(rp.spa + gi);
+        SB = ldg_scale(rp.spb + gi);
+      }
+    }
+  };
+
+  // ---- shared memory ----
+  uint8_t* xs = sm + p.off_x;
+  float* corr = reinterpret_cast<float*>(sm + p.off_corr);
+  int* slot_tile = reinterpret_cast<int*>(sm + p.off_misc);                 // [W]
+  unsigned int* flag = reinterpret_cast<unsigned int*>(sm + p.off_misc + kMaxWarps * 4);
+  unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(sm + p.off_list);
+  unsigned int* ccnt = reinterpret_cast<unsigned int*>(sm + p.off_cnt);      // [2][W][m]
+  const int nunits_c = GW2 ? p.corr_pitch : p.S_real;    // offset-sum units per token
+
+  // This CTA's own shared memory is cleared before the wait for the
+  // preceding kernel: the offset sums (entries of tokens past m stay 0), the
+  // zero region, the candidate counts and thresholds.
+  for (int i = threadIdx.x; i < kMaxTok * nunits_c; i += kThr) corr[i] = 0.f;
+  for (int i = threadIdx.x; i < kZeroBytes / 16; i += kThr)
+    *reinterpret_cast<uint4*>(sm + p.off_zero + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+  if (K > 0)
+    for (int i = threadIdx.x; i < 2 * W * m; i += kThr) ccnt[i] = 0u;
+
+  // With static weights the first run's copies go out before the wait for
+  // the preceding kernel on the stream (which then does not write them);
+  // otherwise after it.
+  const int tile_b = T0 + (rb < re ? rb / rpt : 0);
+  const int r_b = rb < re ? rb % rpt : 0;
+  if (p.early_weights) {
+    const RunPtr r0 = run_ptr(tile_b, r_b, rb < re);
+#pragma unroll
+    for (int j = 0; j < kPD; ++j) copy_step(r0, j);
+  }
+  griddep_launch_dependents();
+  griddep_wait();
+  if (!p.early_weights) {
+    const RunPtr r0 = run_ptr(tile_b, r_b, rb < re);
+#pragma unroll
+    for (int j = 0; j < kPD; ++j) copy_step(r0, j);
+  }
+  __syncthreads();   // the cleared offset sums before the atomics below
+
+  // ---- stage x: token rows of xpitch bytes, 16-byte pieces swizzled by
+  //      token, columns k .. xpitch/2 zero; each piece's offset sum goes to
+  //      its unit (a 64-column half with two group halves, else a step),
+  //      negated ----
+  {
+    const XT* xg = reinterpret_cast<const XT*>(a.x);
+    const int pieces = (int)(p.xpitch / 16);
+    const int kp = k / 8;
+    const int total = m * pieces;
+    constexpr int kB = 8;   // pieces in flight per thread
+    for (int i0 = threadIdx.x; i0 < total; i0 += kB * kThr) {
+      uint4 v[kB];
+      int tk[kB], pc[kB];
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        const int i = i0 + b * kThr;
+        tk[b] = i / pieces;   // one division per piece (a handful per thread)
+        pc[b] = i - tk[b] * pieces;
+        v[b] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < total && pc[b] < kp)
+          v[b] = *reinterpret_cast<const uint4*>(xg + (size_t)tk[b] * k + pc[b] * 8);
+      }
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        if (i0 + b * kThr >= total) continue;
+        if constexpr (kScaledX) {   // elements 2, 3, 6, 7 of each 8 -> x / 16
+          v[b].y = hmul2_u32(v[b].y, 0x2C002C00u);
+          v[b].w = hmul2_u32(v[b].w, 0x2C002C00u);
+        }
+        const uint32_t q = (uint32_t)pc[b];
+        const uint32_t phys = (q & ~7u) | ((q ^ x_swz<GW2>(tk[b])) & 7u);
+        *reinterpret_cast<uint4*>(xs + (size_t)tk[b] * p.xpitch + phys * 16) = v[b];
+        if (kHasOffset && pc[b] < kp) {
+          const float o = offset_sum<BITS, XT>(v[b]);
+          if constexpr (GW2) atomicAdd(&corr[tk[b] * p.corr_pitch + (pc[b] >> 3)], -o);
+          else atomicAdd(&corr[(pc[b] / (kStepCols / 8)) * kMaxTok + tk[b]], -o);
+        }
+      }
+    }
   }
   __syncthreads();
 
-  bool bad = false;
-
-  if (warp == kConsumers) {
-    // ------------------------------ producer ------------------------------
-    if (lane == 0) {
-      prefetch_tmap(&tw);
-      prefetch_tmap(&twb);
-      if (!XRES) prefetch_tmap(&tx);
-      const uint8_t* scales = reinterpret_cast<const uint8_t*>(a.scales);
-      const int xstage = kUnits * p.xbox_bytes;
-      int stage = 0;
-      uint32_t ephase = 0;
-      int j = 0, issued = 0;
-      // Work units: the CTA's first is its own index; later ones come from
-      // the shared counter (CTAs that stream faster take more) or, without
-      // one, in a fixed stride.  The next id is taken when a unit starts, so
-      // the atomic's latency hides behind that unit's copies; an id is only
-      // taken when the CTA has room to process it.
-      int b = (int)blockIdx.x;
-      for (int lb = 0; !bad && b < p.units_total && lb < p.cap_units; ++lb) {
-        int nextb = p.units_total;
-        if (lb + 1 < p.cap_units)
-          nextb = p.sched ? (int)atomicAdd(p.sched, 1u) + (int)gridDim.x : b + (int)gridDim.x;
-        blk_list[lb] = b;
-        const int tb = b * U;
-        const int ntb = min(U, p.tiles_total - tb);
-        const bool sc_bulk = p.scales_aligned && (tb + ntb) * 16 <= n;
-        const uint32_t sbytes = (uint32_t)(ntb * 16 * p.ngroups * 2);
-        for (int c = 0; c < p.chunks; ++c, ++j) {
-          // stage reuse: wait until all consumers released its previous fill
-          if (j >= kStages && !bad) bad = !mbar_wait(&empty[stage], ephase ^ 1u);
-          if (!bad) {
-            blk_stage[stage] = b;
-            uint32_t bytes = (uint32_t)(ntb * kTileBytes);
-            if (!XRES) bytes += (uint32_t)(kUnits * m * 128);
-            if (c == 0 && sc_bulk) bytes += sbytes;
-            mbar_arrive_expect_tx(&full[stage], bytes);
-            uint8_t* wdst = sm + stage * kStageWBytes;
-            if (ntb == kBlockTiles) {
-              tma_load_2d(wdst, &twb, c * (kChunkRowBytes / 4), tb * 16, &full[stage]);
-            } else {
-              for (int t = 0; t < ntb; ++t)
-                tma_load_2d(wdst + t * kTileBytes, &tw, c * (kChunkRowBytes / 4), (tb + t) * 16,
-                            &full[stage]);
-            }
-            if (!XRES) {
-              uint8_t* xdst = sm + p.off_x + stage * xstage;
-              for (int u = 0; u < kUnits; ++u)
-                tma_load_2d(xdst + u * p.xbox_bytes, &tx, c * KC + u * 64, 0, &full[stage]);
-            }
-            if (c == 0 && sc_bulk)
-              bulk_load(sm + p.off_s + (lb % p.nsb) * p.sbuf_bytes,
-                        scales + (size_t)tb * 16 * p.ngroups * 2, sbytes, &full[stage]);
-            issued = j + 1;
-          }
-          if (++stage == kStages) { stage = 0; ephase ^= 1u; }
-        }
-        b = nextb;
-      }
-      // Every copy this CTA issued must have landed before it can finish: the
-      // latest fill of slot s completes phase (fills_of_s - 1) & 1.  On the
-      // normal path the consumers already waited for all of them.
-      for (int s = 0; s < kStages && s < issued; ++s) {
-        const int fills = (issued - 1 - s) / kStages + 1;
-        if (!mbar_wait(&full[s], (uint32_t)((fills - 1) & 1))) bad = true;
-      }
-      // This producer takes no more units (its last take has returned): the
-      // last producer of the grid to get here resets the counter for the
-      // next launch.
-      if (p.sched && atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
-        p.sched[0] = 0u;
-        p.sched[1] = 0u;
-      }
-      // End of work: one more stage, unit id -1, completed by a plain arrive
-      // (after the copies above, so no copy phase is pending on its slot).
-      if (!bad) {
-        if (j >= kStages) bad = !mbar_wait(&empty[stage], ephase ^ 1u);
-        if (!bad) {
-          blk_stage[stage] = -1;
-          mbar_arrive(&full[stage]);
-        }
-      }
-    }
-  } else {
-    // ------------------------------ consumers -----------------------------
-    const int g = lane >> 2, t = lane & 3;
-    const XT* xg = reinterpret_cast<const XT*>(a.x);
-    // (1) resident activations: [unit][token][64] halves, 16-byte pieces
-    //     XOR-swizzled by token so fragment loads avoid bank conflicts.
-    if (XRES) {
-      const int pieces_per_row = k / 8;
-      for (int i = threadIdx.x; i < m * pieces_per_row; i += kConsumers * 32) {
-        const int tok = i / pieces_per_row, pc = i - tok * pieces_per_row;
-        uint4 v = *reinterpret_cast<const uint4*>(xg + (size_t)tok * k + pc * 8);
-        if constexpr (CF::kScaledX) {   // elements 2, 3, 6, 7 of each 8 -> x / 16 (exact)
-          const uint32_t sixteenth = 0x2C002C00u;
-          v.y = hmul2_u32(v.y, sixteenth);
-          v.w = hmul2_u32(v.w, sixteenth);
-        }
-        const int U = pc >> 3, piece = pc & 7;
-        *reinterpret_cast<uint4*>(sm + p.off_x + (U * m + tok) * 128 +
-                                  ((piece ^ (tok & 7)) * 16)) = v;
-      }
-    }
-    // (2) per (token, group): the offset the MMA sums picked up, summed from
-    //     16-byte pieces (the resident copy when there is one, as the MMA
-    //     sees it); absent tokens get 0
-    if constexpr (CF::kCorr) {
-      if (XRES) consumer_sync();
-      const int G = p.gunits * 64;
-      for (int i = m * p.ngroups + threadIdx.x; i < kMaxTok * p.ngroups; i += kConsumers * 32)
-        corr[i] = 0.f;
-      for (int pr = warp; pr < m * p.ngroups; pr += kConsumers) {
-        const int tok = pr / p.ngroups, gidx = pr - tok * p.ngroups;
-        float s = 0.f;
-        for (int e = lane * 8; e < G; e += 256) {
-          const int kk = gidx * G + e;
-          uint4 v;
-          if (XRES) {
-            const int U = kk >> 6, piece = (kk >> 3) & 7;
-            v = *reinterpret_cast<const uint4*>(sm + p.off_x + (U * m + tok) * 128 +
-                                                ((piece ^ (tok & 7)) * 16));
-          } else {
-            v = *reinterpret_cast<const uint4*>(xg + (size_t)tok * k + kk);
-          }
-          s += corr_piece<XT, CF::kScaledX>(v, Codes::kOffset);
-        }
+  // ---- per-lane x addresses (B operand) ----
+  //   column of n-tile nt: GW2: 2 * token + half; else: token.  A lane whose
+  //   column is a token past m reads what a live lane with the same t reads
+  //   (a broadcast; the column is never used).  With GW2, a live column's
+  //   lanes of the other group half must give zeros: they read the zero
+  //   region, at pieces whose banks the live lanes do not use.
+  uint32_t xaddr[NT][kLanePieces];   // step 0's pieces
+  bool xzero[NT];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-        if (lane == 0) corr[pr] = s;
-      }
-    }
-    consumer_sync();
-
-    // per-lane constant shared-memory offsets
-    const int r8 = lane & 7, mi = lane >> 3;
-    uint32_t woff[4];   // ldmatrix address inside a 16-row tile, per unit (int8: per half unit)
+  for (int nt = 0; nt < NT; ++nt) {
+    const int c = 8 * nt + g;
+    int tok = GW2 ? (c >> 1) : c;
+    const bool live = tok < m;
+    if (!live) tok = m - 1;
+    xzero[nt] = GW2 && live && (c & 1) != (t >> 1);
+    const uint32_t sw = x_swz<GW2>(tok);
+    const uint32_t base = sm_base + p.off_x + (uint32_t)tok * p.xpitch;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int seg = (BITS == 4 ? 2 * i : 2 * i) + (mi >> 1);
-      woff[i] = (uint32_t)((r8 + 8 * (mi & 1)) * kChunkRowBytes + ((seg ^ r8) * 16));
+    for (int i = 0; i < kLanePieces; ++i) {
+      const uint32_t pc = (uint32_t)(kLanePieces * t + i);
+      // zero lanes: every step of a run reads within the first kPD * 256 bytes
+      xaddr[nt][i] = xzero[nt] ? sm_base + p.off_zero + ((pc + 2u) & 7u) * 16u
+                               : base + ((pc & ~7u) | ((pc ^ sw) & 7u)) * 16u;
     }
-    uint32_t xoff[NT][4];   // activation piece offsets inside one 64-column unit box
-    bool tok_ok[NT];
+  }
+  // the corr entries of this lane's output columns, for step 0
+  const float* corr_lane[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+    corr_lane[nt] = GW2 ? corr + (t + 4 * nt) * p.corr_pitch : corr + 8 * nt + 2 * t;
+
+  // ---- candidate buffers and thresholds of this warp ----
+  Cands CC{cbuf + (size_t)warp * m * p.cap, ccnt + warp * m, ccnt + W * m + warp * m, p.cap};
+  // thresholds of this lane's tokens (GW2: token t + 4 nt; else 8 nt + 2 t + {0, 1})
+  uint32_t thr[NT][2];
+  auto load_thr = [&]() {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int tok = nt * 8 + g;
-      tok_ok[nt] = tok < m;
-      const int tk = tok < m ? tok : 0;
-#pragma unroll
-      for (int sg = 0; sg < 4; ++sg) {
-        const int piece = BITS == 4 ? (4 * sg + t) : (2 * sg + (t >> 1));
-        xoff[nt][sg] = (uint32_t)(tk * 128 + (((piece & 7) ^ (tk & 7)) * 16) +
-                                  (BITS == 4 ? 0 : (t & 1) * 8));
-      }
+      const int t0 = GW2 ? (t + 4 * nt) : (8 * nt + 2 * t);
+      thr[nt][0] = t0 < m ? CC.thr[t0] : 0xFFFFFFFFu;
+      thr[nt][1] = GW2 ? thr[nt][0] : (t0 + 1 < m ? CC.thr[t0 + 1] : 0xFFFFFFFFu);
     }
-    const uint32_t xunit_stride = XRES ? (uint32_t)(m * 128) : (uint32_t)p.xbox_bytes;
+  };
+  if (K > 0) load_thr();
 
-    int stage = 0;
-    uint32_t fphase = 0;
-    int lb = 0;
-    for (;; ++lb) {
-      // the stage of a unit's first chunk names the unit (-1: no more work)
-      if (!bad) bad = !mbar_wait(&full[stage], fphase);
-      if (bad) break;
-      const int ub = blk_stage[stage];
-      if (ub < 0) break;
-      const int tb = ub * U;
-      const int ntb = min(U, p.tiles_total - tb);
-      const bool active = warp < ntb;
-      const bool sc_bulk = p.scales_aligned && (tb + ntb) * 16 <= n;
-      const int row_a = (tb + warp) * 16 + g, row_b = row_a + 8;
-      const uint16_t* sbuf = reinterpret_cast<const uint16_t*>(sm + p.off_s +
-                                                               (lb % p.nsb) * p.sbuf_bytes);
-      float acc[NT][4], part[NT][4];
+  float acc[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[nt][c] = part[nt][c] = 0.f;
-      uint32_t xb[NT][8];     // B fragments; lanes of absent tokens keep zeros
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) xb[nt][i] = 0u;
-      const uint16_t* srow_a = sc_bulk ? sbuf + (warp * 16 + g) * p.ngroups
-                                       : a.scales + (size_t)min(row_a, n - 1) * p.ngroups;
-      const uint16_t* srow_b = sc_bulk ? sbuf + (warp * 16 + g + 8) * p.ngroups
-                                       : a.scales + (size_t)min(row_b, n - 1) * p.ngroups;
-      const float* corr_t0 = corr + (2 * t) * p.ngroups;      // tokens 2t, 2t+1 (+8 nt)
-      int u_in_group = 0, gi = 0;
+    for (int c = 0; c < 4; ++c) acc[nt][c] = 0.f;
 
-      for (int c = 0; c < p.chunks; ++c) {
-        if (c > 0 && !bad) bad = !mbar_wait(&full[stage], fphase);
-        if (active && !bad) {
-          const uint32_t wst = base + stage * kStageWBytes + warp * kTileBytes;
-          const uint32_t xst = XRES ? base + p.off_x + (uint32_t)(c * kUnits) * xunit_stride
-                                    : base + p.off_x + (uint32_t)(stage * kUnits) * xunit_stride;
-          const int nu = min(kUnits, (k - c * KC) / 64);   // last chunk may be partial
+  const bool head_partial = rb < re && (rb % rpt) != 0 && (rb / rpt + 1) * rpt <= re;
+  const int head_tile = T0 + rb / rpt;
+  const XT* bias = reinterpret_cast<const XT*>(a.bias);
+  XT* logits = reinterpret_cast<XT*>(a.logits);
+  // the head tile's partial sums wait in this lane's stash (shared memory)
+  float* stash = reinterpret_cast<float*>(sm + p.off_misc + 256) +
+                 (size_t)(warp * 32 + lane) * (NT * 4);
+
+  // Store a finished tile's logits; values that reach their token's
+  // threshold go to the warp's candidate buffers.
+  auto finish_tile = [&](int tile, float (&v)[NT][4]) {
+    const int r0 = tile * 16;
+    bool pass[NT][4];
+    unsigned long long key[NT][4];
+    bool any = false;
 #pragma unroll
-          for (int u = 0; u < kUnits; ++u) {
-            if (u < nu) {
-              // ---- activations (B fragments) for this 64-column unit ----
-              const uint32_t xu = xst + u * xunit_stride;
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                if (tok_ok[nt]) {
-                  if constexpr (BITS == 4) {
-#pragma unroll
-                    for (int sg = 0; sg < 2; ++sg) {
-                      const uint4 v = lds128(xu + xoff[nt][sg]);
-                      xb[nt][4 * sg] = v.x; xb[nt][4 * sg + 1] = v.y;
-                      xb[nt][4 * sg + 2] = v.z; xb[nt][4 * sg + 3] = v.w;
-                    }
-                  } else {
-#pragma unroll
-                    for (int sg = 0; sg < 4; ++sg) {
-                      const uint2 v = lds64(xu + xoff[nt][sg]);
-                      xb[nt][2 * sg] = v.x; xb[nt][2 * sg + 1] = v.y;
-                    }
-                  }
-                }
-              }
-              // ---- weights: ldmatrix + offset codes + MMA ----
-              if constexpr (BITS == 4) {
-                uint32_t wv[4];
-                ldmatrix_x4(wv, wst + woff[u]);
-                // wv: (row g, seg 2u), (row g+8, seg 2u), (row g, seg 2u+1), (row g+8, seg 2u+1)
-#pragma unroll
-                for (int sg = 0; sg < 2; ++sg) {
-                  uint32_t qa[4], qb[4];
-                  Codes::run(wv[2 * sg], qa);
-                  Codes::run(wv[2 * sg + 1], qb);
-                  const uint32_t af0[4] = {qa[0], qb[0], qa[1], qb[1]};
-                  const uint32_t af1[4] = {qa[2], qb[2], qa[3], qb[3]};
-#pragma unroll
-                  for (int nt = 0; nt < NT; ++nt) {
-                    Mma16816<XT>::run(part[nt], af0, xb[nt][4 * sg], xb[nt][4 * sg + 1], part[nt]);
-                    Mma16816<XT>::run(part[nt], af1, xb[nt][4 * sg + 2], xb[nt][4 * sg + 3],
-                                      part[nt]);
-                  }
-                }
-              } else {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                  uint32_t wv[4];
-                  ldmatrix_x4(wv, wst + woff[2 * u + hh]);
-#pragma unroll
-                  for (int sg = 0; sg < 2; ++sg) {
-                    uint32_t qa[2], qb[2];
-                    Codes::run(wv[2 * sg], qa);
-                    Codes::run(wv[2 * sg + 1], qb);
-                    const uint32_t af[4] = {qa[0], qb[0], qa[1], qb[1]};
-                    const int s4 = 2 * hh + sg;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                      Mma16816<XT>::run(part[nt], af, xb[nt][2 * s4], xb[nt][2 * s4 + 1],
-                                        part[nt]);
-                  }
-                }
-              }
-              // ---- group end: remove the offset, apply the exact scale ----
-              if (++u_in_group == p.gunits) {
-                u_in_group = 0;
-                const float fa = scale_bits_to_f32<ST>(srow_a[gi]);
-                const float fb = scale_bits_to_f32<ST>(srow_b[gi]);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                  float c0 = 0.f, c1 = 0.f;
-                  if constexpr (CF::kCorr) {
-                    c0 = corr_t0[(nt * 8) * p.ngroups + gi];
-                    c1 = corr_t0[(nt * 8 + 1) * p.ngroups + gi];
-                  }
-                  acc[nt][0] = fmaf(fa, part[nt][0] - c0, acc[nt][0]);
-                  acc[nt][1] = fmaf(fa, part[nt][1] - c1, acc[nt][1]);
-                  acc[nt][2] = fmaf(fb, part[nt][2] - c0, acc[nt][2]);
-                  acc[nt][3] = fmaf(fb, part[nt][3] - c1, acc[nt][3]);
-#pragma unroll
-                  for (int c2 = 0; c2 < 4; ++c2) part[nt][c2] = 0.f;
-                }
-                ++gi;
-              }
-            }
+      for (int c = 0; c < 4; ++c) {
+        pass[nt][c] = false;
+        key[nt][c] = kEmptyKey;
+        if (GW2 && (c & 1)) continue;
+        const int row = r0 + g + 8 * (c >> 1);
+        const int tok = GW2 ? (t + 4 * nt) : (8 * nt + 2 * t + (c & 1));
+        if (row < n && tok < m) {
+          float val = v[nt][c];
+          if (bias) val += to_f32(bias[row]);
+          logits[(size_t)tok * n + row] = from_f32<XT>(val);
+          if (K > 0) {
+            key[nt][c] = topk_key(val, (uint32_t)row);
+            pass[nt][c] = (uint32_t)(key[nt][c] >> 32) >= thr[nt][c & 1];
+            any |= pass[nt][c];
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
-        if (++stage == kStages) { stage = 0; fphase ^= 1u; }
       }
+    }
+    if (K <= 0 || !__any_sync(0xFFFFFFFFu, any)) return;
+    // make room: a token whose buffer could overflow with this tile is
+    // compacted first (raising its threshold), then the values re-checked
+    bool compacted = false;
+    for (int tk = 0; tk < m; ++tk) {
+      if (CC.cnt[tk] + 16u > (unsigned int)CC.cap) {
+        compact(CC, tk, K);
+        compacted = true;
+      }
+    }
+    if (compacted) {
+      load_thr();
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          pass[nt][c] = pass[nt][c] && (uint32_t)(key[nt][c] >> 32) >= thr[nt][c & 1];
+    }
+    // appends, one shared atomic per (value slot, token): lanes of one token
+    // within a value slot share t
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (GW2 && (c & 1)) continue;
+        const unsigned int pm = __ballot_sync(0xFFFFFFFFu, pass[nt][c]);
+        if (pm == 0u) continue;
+        const int tok = GW2 ? (t + 4 * nt) : (8 * nt + 2 * t + (c & 1));
+        const unsigned int peers = pm & (0x11111111u << t);   // same t, passing
+        const int leader = peers ? __ffs(peers) - 1 : 0;
+        unsigned int base = 0u;
+        if (pass[nt][c] && lane == leader) base = atomicAdd(&CC.cnt[tok], (unsigned int)__popc(peers));
+        base = __shfl_sync(0xFFFFFFFFu, base, leader);
+        if (pass[nt][c]) CC.buf[tok * CC.cap + base + __popc(peers & ((1u << lane) - 1u))] = key[nt][c];
+      }
+    __syncwarp();
+  };
 
-      if (active && !bad) {
-        // ---- epilogue: logits (+bias), fp32 copy for the top-K pass ----
-        const int rows[2] = {row_a, row_b};
+  // One step: the stage's weights (copied by this lane), the x pieces, the
+  // MMAs, the scale.
+  auto do_step = [&](int j, const uint32_t (&xq)[NT][kLanePieces], const float* const (&cq)[NT],
+                     uint32_t scA, uint32_t scB) {
+    const uint4 A = lds128(ring + (uint32_t)(2 * j) * 512u);
+    const uint4 B = lds128(ring + (uint32_t)(2 * j + 1) * 512u);
+    float p0[NT][4], p1[NT][4];
+    float c0[NT], c1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float2 cc = *reinterpret_cast<const float2*>(cq[nt] + (GW2 ? 2 * j : j * kMaxTok));
+      c0[nt] = cc.x;
+      c1[nt] = cc.y;
+    }
+    const uint32_t wA[4] = {A.x, A.y, A.z, A.w};
+    const uint32_t wB[4] = {B.x, B.y, B.z, B.w};
+    if constexpr (BITS == 4) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t qa[4], qb[4];
+        Codes::run(wA[i], qa);
+        Codes::run(wB[i], qb);
+        const uint32_t af0[4] = {qa[0], qb[0], qa[1], qb[1]};
+        const uint32_t af1[4] = {qa[2], qb[2], qa[3], qb[3]};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint4 xv = lds128(xq[nt][i] + (uint32_t)j * (xzero[nt] ? 0u : kXStepBytes));
+          float (&pp)[4] = (i & 1) ? p1[nt] : p0[nt];
+          if (i < 2) MmaOp<XT>::first(pp, af0, xv.x, xv.y, i == 0 ? c0[nt] : 0.f, i == 0 ? c1[nt] : 0.f);
+          else MmaOp<XT>::acc(pp, af0, xv.x, xv.y);
+          MmaOp<XT>::acc(pp, af1, xv.z, xv.w);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i2 = 0; i2 < 2; ++i2) {
+        uint4 xv[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          xv[nt] = lds128(xq[nt][i2] + (uint32_t)j * (xzero[nt] ? 0u : kXStepBytes));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t qa[2], qb[2];
+          Codes::run(wA[2 * i2 + h], qa);
+          Codes::run(wB[2 * i2 + h], qb);
+          const uint32_t af[4] = {qa[0], qb[0], qa[1], qb[1]};
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float (&pp)[4] = h ? p1[nt] : p0[nt];
+            const uint32_t b0 = h ? xv[nt].z : xv[nt].x, b1 = h ? xv[nt].w : xv[nt].y;
+            if (i2 == 0) MmaOp<XT>::first(pp, af, b0, b1, h ? 0.f : c0[nt], h ? 0.f : c1[nt]);
+            else MmaOp<XT>::acc(pp, af, b0, b1);
+          }
+        }
+      }
+    }
+    // the exact scale times the step's sum, in fp32
+    if constexpr (GW2) {
+      const float fa0 = scale_bits_to_f32<ST>((uint16_t)(scA & 0xFFFFu));
+      const float fa1 = scale_bits_to_f32<ST>((uint16_t)(scA >> 16));
+      const float fb0 = scale_bits_to_f32<ST>((uint16_t)(scB & 0xFFFFu));
+      const float fb1 = scale_bits_to_f32<ST>((uint16_t)(scB >> 16));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        acc[nt][0] = fmaf(fa0, p0[nt][0] + p1[nt][0], fmaf(fa1, p0[nt][1] + p1[nt][1], acc[nt][0]));
+        acc[nt][2] = fmaf(fb0, p0[nt][2] + p1[nt][2], fmaf(fb1, p0[nt][3] + p1[nt][3], acc[nt][2]));
+      }
+    } else {
+      const float fa = scale_bits_to_f32<ST>((uint16_t)scA);
+      const float fb = scale_bits_to_f32<ST>((uint16_t)scB);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        acc[nt][0] = fmaf(fa, p0[nt][0] + p1[nt][0], acc[nt][0]);
+        acc[nt][1] = fmaf(fa, p0[nt][1] + p1[nt][1], acc[nt][1]);
+        acc[nt][2] = fmaf(fb, p0[nt][2] + p1[nt][2], acc[nt][2]);
+        acc[nt][3] = fmaf(fb, p0[nt][3] + p1[nt][3], acc[nt][3]);
+      }
+    }
+  };
+
+  // ---- main loop over this warp's runs ----
+  int cur_tile = tile_b, cur_r = r_b;
+  RunPtr cur = run_ptr(cur_tile, cur_r, rb < re);
+  uint32_t sa[kPD], sb[kPD];
+#pragma unroll
+  for (int j = 0; j < kPD; ++j) load_scales(cur, j, sa[j], sb[j]);
+  for (int q = rb; q < re; ++q) {
+    // the next run's position (this warp's runs only) and its scales
+    int nx_tile = cur_tile, nx_r = cur_r + 1;
+    if (nx_r == rpt) { nx_r = 0; ++nx_tile; }
+    const RunPtr nxt = nx_r == 0 ? run_ptr(nx_tile, 0, q + 1 < re) : run_next(cur, q + 1 < re);
+    uint32_t sa_n[kPD], sb_n[kPD];
+#pragma unroll
+    for (int j = 0; j < kPD; ++j) load_scales(nxt, j, sa_n[j], sb_n[j]);
+    // this run's x pieces and corr entries
+    uint32_t xq[NT][kLanePieces];
+    const float* cq[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int i = 0; i < kLanePieces; ++i)
+        xq[nt][i] = xzero[nt] ? xaddr[nt][i] : xaddr[nt][i] + (uint32_t)cur.s0 * kXStepBytes;
+      cq[nt] = corr_lane[nt] + (GW2 ? 2 * cur.s0 : cur.s0 * kMaxTok);
+    }
+    if (cur.nsteps == kPD) {
+      // a full run: no per-step checks
+#pragma unroll
+      for (int j = 0; j < kPD; ++j) {
+        cp_async_wait<kPD - 1>();   // this step's copies (kPD - 1 later groups may fly)
+        do_step(j, xq, cq, sa[j], sb[j]);
+        copy_step(nxt, j);          // the stage is free: the next run's step j
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kPD; ++j) {
+        cp_async_wait<kPD - 1>();
+        if (j < cur.nsteps) do_step(j, xq, cq, sa[j], sb[j]);
+        copy_step(nxt, j);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPD; ++j) {
+      sa[j] = sa_n[j];
+      sb[j] = sb_n[j];
+    }
+    // tile end: finish it, or keep it for the merge when it began in a lower warp
+    if (cur_r == rpt - 1) {
+      if (head_partial && cur_tile == head_tile) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int row = rows[c >> 1];
-            const int tok = nt * 8 + 2 * t + (c & 1);
-            if (row < n && tok < m) {
-              float v = acc[nt][c];
-              if (a.bias) v += to_f32(reinterpret_cast<const XT*>(a.bias)[row]);
-              reinterpret_cast<XT*>(a.logits)[(size_t)tok * n + row] = from_f32<XT>(v);
-              if (a.topk > 0) {
-                if (p.vals_stride > 0)
-                  svals[tok * p.vals_stride + lb * U * 16 + (row - tb * 16)] = v;
-                else
-                  a.scratch[(size_t)tok * n + row] = v;
-              }
-            }
-          }
+          for (int c = 0; c < 4; ++c) stash[nt * 4 + c] = acc[nt][c];
+      } else {
+        finish_tile(cur_tile, acc);
       }
-      if (bad) break;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[nt][c] = 0.f;
     }
-    if (threadIdx.x == 0) flags[2] = (unsigned int)lb;   // units this CTA processed
+    cur = nxt;
+    cur_tile = nx_tile;
+    cur_r = nx_r;
   }
+  cp_async_wait<0>();
 
-  if (bad) atomicOr(&flags[0], 1u);
+  // ---- tiles cut between warps: the unfinished one goes to this warp's
+  //      slot (in its own ring, free now) ----
+  // slot of warp w: its own ring region (other warps may still be copying
+  // into theirs), [32 lanes][NT * 4] floats
+  auto slot_of = [&](int w) {
+    return reinterpret_cast<float*>(sm + p.off_ring + (size_t)w * kRingBytes) + lane * (NT * 4);
+  };
+  const bool tail_partial = rb < re && (re % rpt) != 0;
+  // -1: no unfinished tile; -2: no steps at all (skipped by the merge)
+  if (lane == 0) slot_tile[warp] = rb >= re ? -2 : tail_partial ? T0 + (re - 1) / rpt : -1;
+  if (tail_partial) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) slot_of(warp)[nt * 4 + c] = acc[nt][c];
+  }
   __syncthreads();
-  const bool cta_bad = flags[0] != 0u;
-  if (cta_bad && threadIdx.x == 0 && p.err) atomicOr(p.err, 1u);
-  if (a.topk <= 0) return;
-
-  // ---------------- top-K: per-CTA selection, last-CTA merge ----------------
-  SelWork& W = *reinterpret_cast<SelWork*>(sm);
-  const float* sv = p.vals_stride > 0 ? svals : nullptr;
-  const int nunits = (int)flags[2];
-  if (sv) {
-    if (a.topk <= 8)
-      topk_tail<8, XT, true>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
-    else
-      topk_tail<16, XT, true>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
-  } else {
-    if (a.topk <= 8)
-      topk_tail<8, XT, false>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
-    else
-      topk_tail<16, XT, false>(p, W, red, flags, nunits, blk_list, cta_bad, sv);
+  if (head_partial) {
+    float head[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) head[nt][c] = stash[nt * 4 + c];
+    for (int w = warp - 1; w >= 0 && (slot_tile[w] == head_tile || slot_tile[w] == -2); --w) {
+      if (slot_tile[w] == -2) continue;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) head[nt][c] += slot_of(w)[nt * 4 + c];
+    }
+    finish_tile(head_tile, head);
   }
+  if (K <= 0) return;
+
+  // ---- top-K of this CTA ----
+  // Every warp's buffer holds, per token, all of its values that can be
+  // among its K best.  Warp tk takes the K best of the W buffers of token tk
+  // (lane l holds entry l of every buffer) by K rounds of a warp maximum and
+  // writes them, best first, to the CTA's slot in the workspace.
+  __syncthreads();   // every warp's buffers are final
+  for (int tk = warp; tk < m; tk += W) {
+    unsigned long long e[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      const int c = (int)min(ccnt[i * m + tk], (unsigned int)p.cap);
+      e[i] = lane < c ? cbuf[((size_t)i * m + tk) * p.cap + lane] : kEmptyKey;
+    }
+    const unsigned long long mine = warp_tournament<W>(e, K);
+    if (lane < K) a.cand[((size_t)tk * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *flag = (ticket_add(a.counter) == gridDim.x - 1) ? 1u : 0u;
+  __syncthreads();
+  if (*flag == 0u) return;
+
+  // ---- last CTA ----
+  // The slots are sorted and hold disjoint rows, so every slot whose first
+  // entry is below the K-th largest first entry holds nothing of the final
+  // K (K larger keys exist).  Per token: the K best first entries (read in
+  // one round trip, staged in the free ring), then the K x K entries of
+  // their slots (one more), then their K best.
+  const int nsrc = (int)gridDim.x;
+  unsigned long long* heads = reinterpret_cast<unsigned long long*>(sm + p.off_ring);  // [m][nsrc]
+  const bool staged = nsrc <= 256 && (size_t)m * nsrc * 8u <= (size_t)W * kRingBytes;
+  if (staged) {
+    const int total = m * nsrc;
+    constexpr int kB = 8;   // loads per thread in flight
+    for (int i0 = threadIdx.x; i0 < total; i0 += kB * kThr) {
+      unsigned long long v[kB];
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        const int i = i0 + b * kThr;
+        const int tk = i / nsrc;
+        v[b] = i < total ? __ldcg(a.cand + ((size_t)tk * WQL_MAX_CTAS + (i - tk * nsrc)) * K)
+                         : kEmptyKey;
+      }
+#pragma unroll
+      for (int b = 0; b < kB; ++b)
+        if (i0 + b * kThr < total) heads[i0 + b * kThr] = v[b];
+    }
+    __syncthreads();
+  }
+  const int big = p.tex * (p.tpc + 1);   // tiles of the CTAs holding tpc + 1
+  for (int tk = warp; tk < m; tk += W) {
+    const unsigned long long* slots = a.cand + (size_t)tk * WQL_MAX_CTAS * K;
+    unsigned long long mine;
+    if (staged) {
+      unsigned long long e[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        e[q] = lane + 32 * q < nsrc ? heads[tk * nsrc + lane + 32 * q] : kEmptyKey;
+      const unsigned long long hk = warp_tournament<8>(e, K);   // lane r: the r-th best head
+      int sid = -1;                                             // ... and its CTA
+      if (hk != kEmptyKey) {
+        const int tile = key_index(hk) >> 4;
+        sid = tile < big ? tile / (p.tpc + 1) : p.tex + (tile - big) / p.tpc;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int j = lane + 32 * q;          // entry j % K of the (j / K)-th slot
+        const int si = j / K;
+        const int sq = __shfl_sync(0xFFFFFFFFu, sid, si & 31);
+        e[q] = j < K * K && sq >= 0 ? __ldcg(slots + (size_t)sq * K + (j - si * K)) : kEmptyKey;
+      }
+      mine = warp_tournament<8>(e, K);
+    } else {
+      // more slots than staged: every slot, straight from the workspace
+      unsigned long long best[16];
+      warp_topk_of<16>(nsrc * K, K, [&](int i) { return __ldcg(slots + i); }, best);
+      mine = pick(best, lane);
+    }
+    if (lane < K) {
+      a.topk_idx[(size_t)tk * K + lane] = mine != kEmptyKey ? key_index(mine) : -1;
+      a.topk_val[(size_t)tk * K + lane] = mine != kEmptyKey ? key_value(mine) : __int_as_float(0x7FC00000);
+    }
+  }
+  // ready for the next call
+  if (threadIdx.x == 0) *a.counter = 0u;
 }
 
-template <int BITS, typename XT, typename ST, int NT, bool XRES>
-cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& twb, const CUtensorMap& tx,
-                     const DecodeParams& p, size_t smem, int ctas, cudaStream_t s) {
-  auto kern = decode_kernel<BITS, XT, ST, NT, XRES>;
-  static size_t configured = 0;  // per instantiation: raise the smem limit once
+template <int BITS, bool GW2, bool LIN, typename XT, typename ST, int NT>
+cudaError_t launch_t(const DecodeParams& p, size_t smem, int ctas, cudaStream_t s) {
+  auto kern = decode_kernel<BITS, GW2, LIN, XT, ST, NT>;
+  // per instantiation: raise the dynamic smem limit when a launch needs more,
+  // and ask for the smallest shared-memory carveout that holds it, leaving
+  // the rest of the SM's 256 KB to L1 (scale rows are read through L1)
+  static size_t configured = 0;
+  static int carveout = -1;
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  kern<<<ctas, kThreads, smem, s>>>(tw, twb, tx, p);
+  const int pct = (int)(((smem + 1024) * 100 + 228 * 1024 - 1) / (228 * 1024));
+  if (pct != carveout) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         pct > 100 ? 100 : pct);
+    if (e != cudaSuccess) return e;
+    carveout = pct;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(warps_of(NT) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
-// All variants for one activation dtype.
-template <typename XT>
-cudaError_t dispatch_x(const CUtensorMap& tw, const CUtensorMap& twb, const CUtensorMap& tx,
-                       const DecodeParams& p, size_t smem, int ctas, cudaStream_t s) {
-  const bool nt1 = p.a.m <= 8;
-  const bool sf16 = p.a.scale_dtype == WQL_F16;
-#define WQL_DECODE_CASE(B, ST)                                                                \
-  if (p.x_resident) {                                                                        \
-    return nt1 ? launch_t<B, XT, ST, 1, true>(tw, twb, tx, p, smem, ctas, s)                 \
-               : launch_t<B, XT, ST, 2, true>(tw, twb, tx, p, smem, ctas, s);                \
-  }                                                                                          \
-  return nt1 ? launch_t<B, XT, ST, 1, false>(tw, twb, tx, p, smem, ctas, s)                  \
-             : launch_t<B, XT, ST, 2, false>(tw, twb, tx, p, smem, ctas, s);
-  if (p.a.bits == 4) {
-    if (sf16) { WQL_DECODE_CASE(4, __half) }
-    WQL_DECODE_CASE(4, __nv_bfloat16)
+template <bool LIN, typename XT, typename ST>
+cudaError_t dispatch_lin(const DecodeParams& p, bool gw2, int nt, size_t smem, int ctas,
+                         cudaStream_t s) {
+  if (p.a.bits == 4 && gw2) {
+    if (nt == 1) return launch_t<4, true, LIN, XT, ST, 1>(p, smem, ctas, s);
+    if (nt == 2) return launch_t<4, true, LIN, XT, ST, 2>(p, smem, ctas, s);
+    return launch_t<4, true, LIN, XT, ST, 4>(p, smem, ctas, s);
   }
-  if (sf16) { WQL_DECODE_CASE(8, __half) }
-  WQL_DECODE_CASE(8, __nv_bfloat16)
-#undef WQL_DECODE_CASE
+  if (p.a.bits == 4) {
+    if (nt == 1) return launch_t<4, false, LIN, XT, ST, 1>(p, smem, ctas, s);
+    return launch_t<4, false, LIN, XT, ST, 2>(p, smem, ctas, s);
+  }
+  if (nt == 1) return launch_t<8, false, LIN, XT, ST, 1>(p, smem, ctas, s);
+  return launch_t<8, false, LIN, XT, ST, 2>(p, smem, ctas, s);
+}
+
+// Every variant for one activation and scale dtype.
+template <typename XT, typename ST>
+cudaError_t dispatch_xs(const DecodeParams& p, bool gw2, bool lin, int nt, size_t smem, int ctas,
+                        cudaStream_t s) {
+  return lin ? dispatch_lin<true, XT, ST>(p, gw2, nt, smem, ctas, s)
+             : dispatch_lin<false, XT, ST>(p, gw2, nt, smem, ctas, s);
 }
 
 }  // namespace decode_detail

@@ -24,8 +24,9 @@
 // be in flight at the same time (on different streams, or from different
 // host threads without ordering between them) race on it and corrupt each
 // other's results.  Serialise them.
-#include <atomic>
 #include <mutex>
+
+#include <cuda.h>
 
 #include "wql_common.cuh"
 
@@ -33,39 +34,83 @@ namespace wql {
 namespace {
 
 constexpr size_t kAreaBytes = WQL_NOALLOC_SCRATCH_BYTES;
-constexpr int kSliceTokens = 16;                 // token rows per decode launch
-constexpr size_t kSmemBudget = 227 * 1024;
 constexpr int kMaxDevices = 64;
 
 // The scratch area.  Without an initialiser it is zero-filled when the
 // module is loaded and takes no room in the library file.
 static __device__ __align__(256) unsigned char g_noalloc_area[kAreaBytes];
 
-// Device address of the area, per device ordinal; null until looked up.
-std::atomic<void*> g_area_ptr[kMaxDevices];
+// Device address of the area, per device ordinal, with the identity of the
+// context it was looked up in: the address belongs to the module as that
+// context loaded it.  A context torn down and created again (cudaDeviceReset,
+// for one) loads the module afresh, possibly elsewhere, so an address is only
+// reused while the device's current context has the same unique id.
+struct AreaSlot {
+  void* ptr = nullptr;
+  unsigned long long ctx_id = 0;
+};
+AreaSlot g_area[kMaxDevices];
 std::mutex g_setup_mu;
 
-// Address of the area on the current device.  The first call per device does
-// the one-time setup: with that device current, cudaGetSymbolAddress (which
-// also makes the runtime load the module there).  A failed lookup is not
-// cached, so a later call tries again.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+std::once_flag g_ctx_fn_once;
+
+void resolve_ctx_fns() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+  fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_id = reinterpret_cast<CtxGetIdFn>(fn);
+}
+
+// Unique id of the calling thread's current context (0 if none).
+cudaError_t current_ctx_id(unsigned long long* id) {
+  std::call_once(g_ctx_fn_once, resolve_ctx_fns);
+  if (!g_ctx_current || !g_ctx_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  *id = 0;
+  if (ctx && g_ctx_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
+
+// Address of the area on the current device.  The set-up -- with that device
+// current, cudaGetSymbolAddress, which also makes the runtime load the module
+// there -- runs on the first call per device and again whenever the device's
+// context has been replaced since.  A failed lookup is not kept, so a later
+// call tries again.
 cudaError_t area_on_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  void* p = g_area_ptr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    p = g_area_ptr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-      e = cudaGetSymbolAddress(&p, g_noalloc_area);
-      if (e != cudaSuccess) return e;
-      if (p == nullptr) return cudaErrorInvalidSymbol;
-      g_area_ptr[dev].store(p, std::memory_order_release);
-    }
+  // id 0: no context is current yet on this thread (the lookup below makes
+  // the device's primary context current, and its id is read after it)
+  unsigned long long id = 0;
+  e = current_ctx_id(&id);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  AreaSlot& slot = g_area[dev];
+  if (slot.ptr == nullptr || slot.ctx_id != id) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_area);
+    if (e != cudaSuccess) return e;
+    if (p == nullptr) return cudaErrorInvalidSymbol;
+    e = current_ctx_id(&id);
+    if (e != cudaSuccess) return e;
+    slot.ptr = p;
+    slot.ctx_id = id;
   }
-  *out = p;
+  *out = slot.ptr;
   return cudaSuccess;
 }
 
@@ -101,9 +146,9 @@ extern "C" wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t
       !is_aligned(logits_out, 2) || !is_aligned(bias, 2))
     return WQL_EUNSUPPORTED;
   if (m == 0 || n == 0) return WQL_OK;
-  const int64_t slice_max = m < kSliceTokens ? m : kSliceTokens;
-  if (decode_smem_bytes((int)slice_max, (int)k, w->bits, (int)g) > kSmemBudget)
-    return WQL_EUNSUPPORTED;
+  const int slice_tokens = decode_max_tokens((int)k, w->bits, (int)g, topk);
+  if (slice_tokens < 1) return WQL_EUNSUPPORTED;
+  const int64_t slice_max = m < slice_tokens ? m : slice_tokens;
   // Every slice reuses the same area, so one slice's layout is the need.
   const WorkspaceLayout lay = workspace_layout(slice_max, n, topk);
   if (lay.total > kAreaBytes) return WQL_EWORKSPACE;
@@ -133,11 +178,10 @@ extern "C" wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t
   base.counter = counter;   // also schedules the decode kernel's work units
   if (topk > 0) {
     base.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
-    base.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
   }
   const size_t esz = 2;
-  for (int64_t m0 = 0; m0 < m; m0 += kSliceTokens) {
-    const int64_t mc = (m - m0) < kSliceTokens ? (m - m0) : kSliceTokens;
+  for (int64_t m0 = 0; m0 < m; m0 += slice_tokens) {
+    const int64_t mc = (m - m0) < slice_tokens ? (m - m0) : slice_tokens;
     LogitsArgs a = base;
     a.x = static_cast<const unsigned char*>(x) + (size_t)m0 * (size_t)k * esz;
     a.m = (int)mc;

@@ -55,7 +55,6 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 thread_local std::string g_last_error;
 constexpr int kDecodeMaxTokens = 16;
-constexpr size_t kDecodeSmemBudget = 227 * 1024;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool half_dtype(int d) { return d == WQL_F16 || d == WQL_BF16; }
@@ -96,8 +95,7 @@ WorkspaceLayout workspace_layout(int64_t m, int64_t n, int32_t topk) {
   if (topk > 0) off += 256 * sizeof(unsigned int);
   l.cand_off = off;
   if (topk > 0) off += round_up((size_t)m * WQL_MAX_CTAS * (size_t)topk * 8, 256);
-  l.scratch_off = off;
-  if (topk > 0) off += round_up((size_t)m * (size_t)n * 4, 256);
+  (void)n;
   l.total = off;
   return l;
 }
@@ -207,13 +205,15 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
     return WQL_EUNSUPPORTED;
   if (m == 0 || n == 0) return WQL_OK;
   const WorkspaceLayout lay = workspace_layout(m, n, topk);
-  if (topk > 0 && (!workspace || ws_bytes < lay.total || !aligned(workspace, 256)))
-    return WQL_EWORKSPACE;
+  // top-K needs a workspace; any workspace given (top-K or not) holds the
+  // kernels' counter block, so it must be large enough and aligned
+  if (topk > 0 && !workspace) return WQL_EWORKSPACE;
+  if (workspace && (ws_bytes < lay.total || !aligned(workspace, 256))) return WQL_EWORKSPACE;
   const int esz = 2;
-  const int64_t dchunk = kDecodeMaxTokens;   // tokens per decode launch
-  if (decode_smem_bytes((int)(m < dchunk ? m : dchunk), (int)k, w->bits, (int)g) >
-      kDecodeSmemBudget)
-    return WQL_EUNSUPPORTED;
+  // tokens per decode launch: 16, fewer when x for 16 rows does not fit in
+  // shared memory next to the rest
+  const int dchunk = decode_max_tokens((int)k, w->bits, (int)g, topk);
+  if (dchunk < 1) return WQL_EUNSUPPORTED;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   // No workspace (allowed when topk == 0): the kernels skip the error word.
@@ -234,7 +234,6 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   if (ws) base.counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
   if (topk > 0) {
     base.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
-    base.scratch = reinterpret_cast<float*>(ws + lay.scratch_off);
     base.tickets = reinterpret_cast<unsigned int*>(ws + lay.tickets_off);
   }
   // Token counts above 16 go to the tensor-core kernel (up to 256 tokens per
@@ -243,7 +242,7 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   LogitsArgs probe = base;
   probe.m = (int)(m < 256 ? m : 256);
   const bool use_tc = m > kDecodeMaxTokens && tc_supported(probe);
-  const int64_t chunk = use_tc ? 256 : kDecodeMaxTokens;
+  const int64_t chunk = use_tc ? 256 : dchunk;
   for (int64_t m0 = 0; m0 < m; m0 += chunk) {
     const int64_t mc = (m - m0) < chunk ? (m - m0) : chunk;
     LogitsArgs a = base;

@@ -426,14 +426,17 @@ struct LogitsArgs {
   float* topk_val;
   unsigned int* counter;      // zero between calls; the last CTA resets it
   unsigned long long* cand;   // [m][WQL_MAX_CTAS][topk] keys
-  float* scratch;             // [m][n] fp32 logits (top-K input, decode path)
   unsigned int* tickets;      // [256] per-token tickets of the top-K selection
                               // (zero between calls)
+  int weights_static;         // 1: no kernel that may precede this launch on the
+                              // stream writes qweight / scales
 };
-// Bandwidth-bound path for m <= 16 (TMA-fed warp MMA, split over vocab rows).
-// `err` is the workspace's sticky error word.
+// Bandwidth-bound path for m <= 16 (warp MMA fed straight from global memory,
+// split over vocab rows).  `err` is the workspace's sticky error word.
 cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s);
-size_t decode_smem_bytes(int m, int k, int bits, int group_eff);
+size_t decode_smem_bytes(int m, int k, int bits, int group_eff, int topk);
+// Most token rows one decode launch takes for this shape (0: none fits).
+int decode_max_tokens(int k, int bits, int group_eff, int topk);
 // Tensor-core path for 16 < m <= 256 (fp16 activations and scales): logits
 // only (a.topk is ignored; launch_topk_select follows it).
 bool tc_supported(const LogitsArgs& a);
@@ -457,7 +460,7 @@ cudaError_t launch_rescore(const RescoreArgs& a, cudaStream_t s);
 
 // Workspace layout shared by the launchers and wql_workspace_size().
 struct WorkspaceLayout {
-  size_t counter_off, tickets_off, cand_off, scratch_off, total;
+  size_t counter_off, tickets_off, cand_off, total;
 };
 WorkspaceLayout workspace_layout(int64_t m, int64_t n, int32_t topk);
 
