@@ -19,6 +19,14 @@ copied back every step.  `--gpus N`
 under torchrun runs N independent replicas (the head is replicated, not
 sharded) and reports the units of all ranks over the slowest rank's time.
 
+The same line carries a `configs` block: every head of the metric at each
+token count it is quoted at -- the 50304 x 512 W4-g64 head (L2-resident),
+the 151936 x 1024 W4-g64 and W8-g128 heads at M = 1/32/256, the 248320 x
+5120 int4-g128 MSE head at M = 1..5 and 16, and the int8 per-row head with
+top-8 rescoring and its greedy-token agreement counts -- each call's median
+and 10th-percentile device time over 120 calls, with its own clock record;
+and `roofline_decode_m1`, the decode kernel alone at M = 1 with top-K off.
+
 `--impl reference` times the CPU oracle (the slow binary64 C restatement) on
 a bounded row sample of the same workload and prints the same JSON line with
 "impl": "reference".
@@ -362,6 +370,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
         return None
 
     pk = peaks()
+    configs = None if args.no_configs else run_configs(dev, stream, pk)
     value = job_throughput_gbs(step_bytes(MS), args.steps, world, dev_s)
     med = {m: statistics.median(logit_us[m]) for m in MS}   # each entry: mean of R calls
     calls = {}
@@ -400,6 +409,20 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
                 "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
                 "kernel": kern, "call": f"M={dom_m}, top-K off", "launch_us": round(dom_us, 2),
                 "peak_note": f"{pk['source']} copy"}
+    # the decode kernel at M = 1 with top-K off: one launch per call, so the
+    # per-call time of the W4 head is that kernel's launch duration
+    roof_m1 = None
+    if configs is not None:
+        c = configs["C2"]["calls"]["M1_top0"]
+        src_d = kernel_src_hash(["decode_impl.cuh", "decode.cu", "wql_common.cuh", "sm100.cuh"])
+        roof_m1 = {"bound": "hbm", "achieved": c["GBps"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                   "frac": round(c["GBps"] / pk["hbm_gbs"], 4),
+                   "frac_of_spec": round(c["GBps"] / SPEC_HBM_GBS, 4),
+                   "traffic": recorded_traffic("decode_kernel", "M1", src_d),
+                   "kernel": "decode_kernel", "call": "151936x1024 W4-g64, M=1, top-K off",
+                   "launch_us_median": c["us_median"], "launch_us_p10": c["us_p10"],
+                   "algorithmic_bytes": c["bytes"],
+                   "peak_note": f"{pk['source']} copy; spec {SPEC_HBM_GBS:.0f} GB/s"}
     return {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -416,6 +439,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
                              "roofline: graphs of 20 calls; e2e: eager public-API calls"},
         "calls": calls, "quantize_ms": round(quant_ms, 3),
         "roofline": roof,
+        "roofline_decode_m1": roof_m1,
+        "configs": configs,
         "cpu_baseline": None,
         "e2e": {"value": round(job_throughput_gbs(step_bytes(MS), args.steps, world, e2e_s), 1),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -426,10 +451,146 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> dict | None:
 
 
 # ---------------------------------------------------------------------------
+# Every workload of the metric: per-call times of each head and token count
+# ---------------------------------------------------------------------------
+
+SPEC_HBM_GBS = 8000.0     # GB300 HBM3e nominal rate (context beside the measured copy rate)
+
+
+def call_stats(per_call_us: list[float]) -> dict:
+    """Median and 10th percentile of the per-call samples."""
+    v = sorted(per_call_us)
+    p10 = v[max(0, int(math.floor(0.1 * (len(v) - 1))))]
+    return {"us_median": round(statistics.median(v), 2), "us_p10": round(p10, 2)}
+
+
+def run_configs(dev, stream, pk: dict, calls_per_sample: int = 12, samples: int = 10) -> dict:
+    """Each head of the metric at each token count it is quoted at: device
+    time per wql_logits call (top-K off and top-8), as CUDA-graph replays of
+    `calls_per_sample` consecutive calls that rotate over weight copies, so
+    every call but the small head's reads its weights from HBM.  Each sample
+    is one replay's mean per call; `samples` replays give median and p10
+    over samples x calls_per_sample calls."""
+    import torch
+    import weight_only_quantized_wql_gb300 as wql
+    from weight_only_quantized_wql_gb300 import synth
+
+    R = calls_per_sample
+    cap = torch.cuda.Stream(dev)
+    ws = wql.Workspace(dev)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                fn()
+        stream.wait_stream(cap)
+        return g
+
+    def time_calls(x, copies, topk, n):
+        out = torch.empty(x.shape[0], n, dtype=x.dtype, device=dev)
+        idx = torch.empty(x.shape[0], max(topk, 1), dtype=torch.int32, device=dev)
+        val = torch.empty(x.shape[0], max(topk, 1), dtype=torch.float32, device=dev)
+
+        def fn():
+            for r in range(R):
+                c = copies[r % len(copies)]
+                if topk:
+                    wql.wql_logits(x, c, topk=topk, workspace=ws, out=out, topk_idx=idx,
+                                   topk_val=val)
+                else:
+                    wql.wql_logits(x, c, topk=0, workspace=ws, out=out)
+        fn()
+        torch.cuda.synchronize()
+        g = capture(fn)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(samples):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            per.append(a.elapsed_time(b) * 1e3 / R)
+        del g
+        return per
+
+    def entry(wl, m, topk, copies, x):
+        st = call_stats(time_calls(x, copies, topk, wl.n))
+        b = logits_bytes(m, wl.n, wl.k, wl.bits, wl.group, topk=topk)
+        gbs = b / (st["us_median"] * 1e-6) / 1e9
+        e = dict(st, n_calls=R * samples, bytes=b, GBps=round(gbs, 1),
+                 frac_hbm=round(gbs / pk["hbm_gbs"], 3),
+                 frac_hbm_spec=round(gbs / SPEC_HBM_GBS, 3))
+        if m >= 32:
+            tfl = 2.0 * m * wl.n * wl.k / (st["us_median"] * 1e-6) / 1e12
+            e.update(TFLOPs=round(tfl, 1), frac_tensor=round(tfl / pk["bf16_tflops"], 3))
+        return e
+
+    def make_head(wl, ncopies):
+        w = synth.weight(wl.n, wl.k, wl.w_dtype, seed=wl.w_seed, device=dev)
+        sdt = torch.float16 if wl.scale_dtype == synth.F16 else torch.bfloat16
+        wql.wql_quantize(w[:256], wl.bits, wl.group, sdt, wl.clip)   # load the kernel
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        qw = wql.wql_quantize(w, wl.bits, wl.group, sdt, wl.clip)
+        b.record(stream)
+        torch.cuda.synchronize()
+        qms = a.elapsed_time(b)
+        copies = [qw] + [wql.QuantizedWeight(qw.qweight.clone(), qw.scales.clone(), qw.bits,
+                                             qw.group, qw.n, qw.k) for _ in range(ncopies - 1)]
+        return w, copies, qms
+
+    def head_block(key, ncopies, topks, label):
+        wl = synth.WORKLOADS[key]
+        w, copies, qms = make_head(wl, ncopies)
+        del w
+        wbytes = copies[0].qweight.numel() * copies[0].qweight.element_size() + \
+            copies[0].scales.numel() * 2
+        blk = {"workload": key, "n": wl.n, "k": wl.k, "bits": wl.bits,
+               "group": wl.group or "row", "clip": "mse" if wl.clip else "rtn",
+               "weight_copies": ncopies, "weight_bytes": wbytes, "quantize_ms": round(qms, 2),
+               "l2": label, "calls": {}}
+        for m in wl.ms:
+            x = synth.activations(m, wl.k, wl.x_dtype, seed=1000 + m, device=dev)
+            for topk in topks(m):
+                blk["calls"][f"M{m}_top{topk}"] = entry(wl, m, topk, copies, x)
+        del copies
+        torch.cuda.empty_cache()
+        return blk
+
+    hbm = "inputs larger than L2: rotating weight copies, each call reads a copy that " \
+          "the call before it did not"
+    res = {"timing": f"CUDA-graph replays of {R} consecutive calls; each sample one replay's "
+                     f"mean per call; median and p10 over {samples} samples "
+                     f"({R * samples} calls)",
+           "peak_hbm_gbs": pk["hbm_gbs"], "spec_hbm_gbs": SPEC_HBM_GBS}
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    res["C1"] = head_block("pr_fixture_50304x512_w4g64", 1, lambda m: (0, 8),
+                           "L2-resident: the 12.9 MB head stays in the 129 MB L2 between calls")
+    res["C2"] = head_block("qwen_151936x1024_w4g64", 4, lambda m: (0, 8), hbm)
+    res["C3"] = head_block("qwen_151936x1024_w8g128", 2, lambda m: (0, 8), hbm)
+    res["C5"] = head_block("head_248320x5120_w4g128_mse", 2,
+                           lambda m: (0, 8) if m == 1 else (8,), hbm)
+    res["C4"] = argmax_study(dev)
+    res["clocks"] = clocks.stop()
+    return res
+
+
+# ---------------------------------------------------------------------------
 # Argmax study: int8 per-row head, M = 1 rows, top-8 rescoring
 # ---------------------------------------------------------------------------
 
 def run_argmax_study(args) -> dict:
+    import torch
+    return argmax_study(torch.device("cuda", 0))
+
+
+def argmax_study(dev) -> dict:
     """The 151936 x 2048 int8 per-row head with an fp16 reference weight
     ("Fused WNA16 GEMM for tied quantized lm_head logits", reviewer comment
     items 1-2): 4096 seeded rows, each an M = 1 wql_logits call with top-8
@@ -446,7 +607,6 @@ def run_argmax_study(args) -> dict:
     from weight_only_quantized_wql_gb300 import synth
 
     wl = synth.WORKLOADS["qwen_151936x2048_w8row_rescore"]
-    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     wql.load()
     stream = torch.cuda.current_stream(dev)
@@ -715,6 +875,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload block (all five heads at each token count)")
     ap.add_argument("--study", choices=["argmax", "embed"], default=None,
                     help="argmax: the int8 per-row head's greedy-token agreement study; "
                          "embed: the tied-embedding gather (each a separate JSON line, "

@@ -44,12 +44,14 @@
 //    lower bound of the final K-th value).  A finished tile's values are
 //    compared against the threshold; the few that reach it are appended.  A
 //    buffer about to overflow is compacted to its K best, which raises the
-//    threshold.  At the end, per token, one warp takes the K best of the
-//    W buffers (K rounds of a warp maximum) and writes them, sorted, to the
-//    CTA's slot of the workspace.  The last CTA to take the ticket (acquire-
-//    release atomic) reads every slot's first entry; only the slots holding
-//    the K largest first entries can hold any of the final K, so it reads
-//    those K slots and takes the K best of their K x K entries.
+//    threshold.  At the end the CTA takes, per token, the K best of its
+//    warps' buffers (K rounds of a warp maximum: over each warp's sorted K
+//    best, merged from registers, with one or two tokens; over all buffers
+//    at once with more) and writes them, sorted, to its slot of the
+//    workspace.  The last CTA to take the ticket (acquire-release atomic)
+//    reads every slot's first entry; only the slots holding the K largest
+//    first entries can hold any of the final K, so it merges those K sorted
+//    slots.
 //  * Programmatic dependent launch: the kernel lets the next kernel on the
 //    stream launch early and reads x, the workspace and the outputs only
 //    after griddepcontrol.wait.  With static weights (LogitsArgs::
@@ -212,29 +214,6 @@ __device__ __forceinline__ uint32_t value_key(float v) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Rank (0 = largest) of `key` among the c keys at s (shared memory, 16-byte
-// aligned, keys unique): how many are larger.  Every lane reads the same
-// addresses (broadcasts), which costs far less than shuffling keys around
-// the warp.
-__device__ __forceinline__ int rank_smem(const unsigned long long* s, int c,
-                                         unsigned long long key) {
-  int r = 0;
-  // eight 16-byte loads in flight before any compare (each is a broadcast)
-  for (int j0 = 0; j0 < c; j0 += 16) {
-    ulonglong2 v[8];
-#pragma unroll
-    for (int b = 0; b < 8; ++b)
-      v[b] = j0 + 2 * b < c ? *reinterpret_cast<const ulonglong2*>(s + j0 + 2 * b)
-                            : make_ulonglong2(0ull, 0ull);
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int j = j0 + 2 * b;
-      r += (j < c && v[b].x > key ? 1 : 0) + (j + 1 < c && v[b].y > key ? 1 : 0);
-    }
-  }
-  return r;
-}
-
 // The K best of `count` keys load(i), by one warp (each lane a register
 // list, then the lanes merged); returned on every lane in `out`.
 template <int KT, typename Load>
@@ -286,6 +265,30 @@ __device__ __forceinline__ unsigned long long warp_tournament(unsigned long long
   return mine;
 }
 
+// The K best of up to 32 sorted lists (descending, kEmptyKey-padded), lane
+// l holding list l in registers: K rounds of a warp maximum over the lists'
+// heads; the winning lane shifts its list.  The r-th best ends on lane r.
+template <int KT>
+__device__ __forceinline__ unsigned long long warp_merge_lists(unsigned long long (&lst)[KT],
+                                                               int K) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long mine = kEmptyKey;
+  for (int r = 0; r < K; ++r) {
+    const unsigned long long head = lst[0];
+    const uint32_t hi = (uint32_t)(head >> 32);
+    const uint32_t mh = redux_max_u32(hi);
+    const uint32_t ml = redux_max_u32(hi == mh ? (uint32_t)head : 0u);
+    const unsigned long long top = ((unsigned long long)mh << 32) | ml;
+    if (lane == r) mine = top;
+    if (head == top && top != kEmptyKey) {
+#pragma unroll
+      for (int i = 0; i < KT - 1; ++i) lst[i] = lst[i + 1];
+      lst[KT - 1] = kEmptyKey;
+    }
+  }
+  return mine;
+}
+
 // Ticket of the last-CTA merge: an atomic add whose release makes this CTA's
 // slot writes and threshold update (ordered before it by the preceding block
 // barrier) visible before the ticket, and whose acquire, for the last CTA,
@@ -306,22 +309,35 @@ struct Cands {
   int cap;
 };
 
-// Reduce token tk's buffer to its K best (one key per lane, cap <= 32), set
-// the count to min(count, K) and the threshold to the K-th best's value key
-// when there are K.  One shared copy of the code for every call site (kept
-// warm in the instruction cache by the compactions during the main loop).
-// (Arguments by value: a reference would put them in local memory.)
+// Reduce a buffer (one of a warp's, or any run of at most 32 keys in shared
+// memory) to its K best, sorted best first (kEmptyKey past the count): K
+// rounds of a warp maximum over one key per lane.  Sets the count to
+// min(count, K) and, with K keys, the threshold to the K-th best's value
+// key.  One copy of the code for every call site.  (Arguments by value: a
+// reference would put them in local memory.)
 static __device__ __noinline__ void compact_buf(unsigned long long* b, unsigned int* cnt,
                                                 unsigned int* thr, int cap, int K) {
   const int lane = threadIdx.x & 31;
   const int c = (int)min(*cnt, (unsigned int)cap);
-  const unsigned long long key = lane < c ? b[lane] : kEmptyKey;
-  const int rank = lane < c ? rank_smem(b, c, key) : 32;
+  unsigned long long e[1] = {lane < c ? b[lane] : kEmptyKey};
+  const unsigned long long mine = warp_tournament<1>(e, K);
   __syncwarp();
-  if (rank < K) b[rank] = key;
+  if (lane < K) b[lane] = mine;
   if (lane == 0) *cnt = (unsigned int)min(c, K);
-  if (rank == K - 1) *thr = (uint32_t)(key >> 32);
+  if (lane == K - 1 && c >= K) *thr = (uint32_t)(mine >> 32);
   __syncwarp();
+}
+
+// The K best of up to 32 sorted lists (descending), lane l passing its own
+// list and length (0: none; shared or global memory): K rounds of a warp
+// maximum over the lists' heads, the lists held in registers.  The r-th
+// best ends on lane r.  One copy of the code for every call site.
+static __device__ __noinline__ unsigned long long merge_lists(const unsigned long long* lst_p,
+                                                              int len, int K) {
+  unsigned long long lst[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) lst[j] = j < len ? lst_p[j] : kEmptyKey;
+  return warp_merge_lists<16>(lst, K);
 }
 __device__ __forceinline__ void compact(const Cands& C, int tk, int K) {
   compact_buf(C.buf + tk * C.cap, C.cnt + tk, C.thr + tk, C.cap, K);
@@ -840,19 +856,32 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
 
   // ---- top-K of this CTA ----
   // Every warp's buffer holds, per token, all of its values that can be
-  // among its K best.  Warp tk takes the K best of the W buffers of token tk
-  // (lane l holds entry l of every buffer) by K rounds of a warp maximum and
-  // writes them, best first, to the CTA's slot in the workspace.
+  // among its K best.  With up to four tokens each warp sorts its own
+  // buffers' K best (a compaction), then warp tk merges the W sorted lists
+  // of token tk; with more tokens warp tk takes the K best of the W buffers
+  // at once (lane l holding entry l of every buffer).  The CTA's K best go,
+  // best first, to its slot in the workspace.
   __syncthreads();   // every warp's buffers are final
-  for (int tk = warp; tk < m; tk += W) {
-    unsigned long long e[W];
-#pragma unroll
-    for (int i = 0; i < W; ++i) {
-      const int c = (int)min(ccnt[i * m + tk], (unsigned int)p.cap);
-      e[i] = lane < c ? cbuf[((size_t)i * m + tk) * p.cap + lane] : kEmptyKey;
+  if (m <= 4) {
+    for (int tk = 0; tk < m; ++tk) compact(CC, tk, K);
+    __syncthreads();
+    for (int tk = warp; tk < m; tk += W) {
+      const int len = lane < W ? (int)ccnt[lane * m + tk] : 0;
+      const unsigned long long mine =
+          merge_lists(cbuf + ((size_t)(lane < W ? lane : 0) * m + tk) * p.cap, len, K);
+      if (lane < K) a.cand[((size_t)tk * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
     }
-    const unsigned long long mine = warp_tournament<W>(e, K);
-    if (lane < K) a.cand[((size_t)tk * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
+  } else {
+    for (int tk = warp; tk < m; tk += W) {
+      unsigned long long e[W];
+#pragma unroll
+      for (int i = 0; i < W; ++i) {
+        const int c = (int)min(ccnt[i * m + tk], (unsigned int)p.cap);
+        e[i] = lane < c ? cbuf[((size_t)i * m + tk) * p.cap + lane] : kEmptyKey;
+      }
+      const unsigned long long mine = warp_tournament<W>(e, K);
+      if (lane < K) a.cand[((size_t)tk * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) *flag = (ticket_add(a.counter) == gridDim.x - 1) ? 1u : 0u;
@@ -862,28 +891,37 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
   // ---- last CTA ----
   // The slots are sorted and hold disjoint rows, so every slot whose first
   // entry is below the K-th largest first entry holds nothing of the final
-  // K (K larger keys exist).  Per token: the K best first entries (read in
-  // one round trip, staged in the free ring), then the K x K entries of
-  // their slots (one more), then their K best.
+  // K (K larger keys exist).  Per token: every slot's first entry (one round
+  // trip, staged in the free ring in runs of 32), each run's K best
+  // (compactions), their merge -- the K best first entries -- and the merge
+  // of those K slots.
   const int nsrc = (int)gridDim.x;
-  unsigned long long* heads = reinterpret_cast<unsigned long long*>(sm + p.off_ring);  // [m][nsrc]
-  const bool staged = nsrc <= 256 && (size_t)m * nsrc * 8u <= (size_t)W * kRingBytes;
+  const int nch = (nsrc + 31) / 32;                     // runs of 32 first entries per token
+  unsigned long long* heads = reinterpret_cast<unsigned long long*>(sm + p.off_ring);  // [m][nch][32]
+  unsigned int* hcnt = reinterpret_cast<unsigned int*>(heads + (size_t)m * nch * 32);  // [m][nch]
+  unsigned int* hthr = hcnt + m * nch;
+  const bool staged = nch <= 32 &&
+      (size_t)m * nch * (32 * 8 + 8) <= (size_t)W * kRingBytes;
   if (staged) {
-    const int total = m * nsrc;
+    const int total = m * nch * 32;
     constexpr int kB = 8;   // loads per thread in flight
     for (int i0 = threadIdx.x; i0 < total; i0 += kB * kThr) {
       unsigned long long v[kB];
 #pragma unroll
       for (int b = 0; b < kB; ++b) {
         const int i = i0 + b * kThr;
-        const int tk = i / nsrc;
-        v[b] = i < total ? __ldcg(a.cand + ((size_t)tk * WQL_MAX_CTAS + (i - tk * nsrc)) * K)
-                         : kEmptyKey;
+        const int tk = i / (nch * 32), src = i - tk * nch * 32;
+        v[b] = i < total && src < nsrc
+                   ? __ldcg(a.cand + ((size_t)tk * WQL_MAX_CTAS + src) * K) : kEmptyKey;
       }
 #pragma unroll
       for (int b = 0; b < kB; ++b)
         if (i0 + b * kThr < total) heads[i0 + b * kThr] = v[b];
     }
+    for (int i = threadIdx.x; i < m * nch; i += kThr)
+      hcnt[i] = (unsigned int)min(32, nsrc - (i % nch) * 32);
+    __syncthreads();
+    for (int i = warp; i < m * nch; i += W) compact_buf(heads + (size_t)i * 32, hcnt + i, hthr + i, 32, K);
     __syncthreads();
   }
   const int big = p.tex * (p.tpc + 1);   // tiles of the CTAs holding tpc + 1
@@ -891,24 +929,14 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
     const unsigned long long* slots = a.cand + (size_t)tk * WQL_MAX_CTAS * K;
     unsigned long long mine;
     if (staged) {
-      unsigned long long e[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        e[q] = lane + 32 * q < nsrc ? heads[tk * nsrc + lane + 32 * q] : kEmptyKey;
-      const unsigned long long hk = warp_tournament<8>(e, K);   // lane r: the r-th best head
-      int sid = -1;                                             // ... and its CTA
+      const int c = lane < nch ? tk * nch + lane : 0;
+      const unsigned long long hk = merge_lists(heads + (size_t)c * 32, lane < nch ? (int)hcnt[c] : 0, K);
+      int sid = -1;            // lane r: the CTA of the r-th best first entry
       if (hk != kEmptyKey) {
         const int tile = key_index(hk) >> 4;
         sid = tile < big ? tile / (p.tpc + 1) : p.tex + (tile - big) / p.tpc;
       }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int j = lane + 32 * q;          // entry j % K of the (j / K)-th slot
-        const int si = j / K;
-        const int sq = __shfl_sync(0xFFFFFFFFu, sid, si & 31);
-        e[q] = j < K * K && sq >= 0 ? __ldcg(slots + (size_t)sq * K + (j - si * K)) : kEmptyKey;
-      }
-      mine = warp_tournament<8>(e, K);
+      mine = merge_lists(slots + (size_t)(sid >= 0 ? sid : 0) * K, sid >= 0 ? K : 0, K);
     } else {
       // more slots than staged: every slot, straight from the workspace
       unsigned long long best[16];
