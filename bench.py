@@ -518,9 +518,10 @@ def run_configs(dev, stream, pk: dict, calls_per_sample: int = 12, samples: int 
         del g
         return per
 
-    def entry(wl, m, topk, copies, x):
+    def entry(wl, m, topk, copies, x, bits, group, wbytes):
         st = call_stats(time_calls(x, copies, topk, wl.n))
-        b = logits_bytes(m, wl.n, wl.k, wl.bits, wl.group, topk=topk)
+        # the weight as stored (codes, scales, zero points) + X + logits + top-K
+        b = wbytes + m * wl.k * 2 + m * wl.n * 2 + m * topk * 8
         gbs = b / (st["us_median"] * 1e-6) / 1e9
         e = dict(st, n_calls=R * samples, bytes=b, GBps=round(gbs, 1),
                  frac_hbm=round(gbs / pk["hbm_gbs"], 3),
@@ -530,34 +531,41 @@ def run_configs(dev, stream, pk: dict, calls_per_sample: int = 12, samples: int 
             e.update(TFLOPs=round(tfl, 1), frac_tensor=round(tfl / pk["bf16_tflops"], 3))
         return e
 
-    def make_head(wl, ncopies):
+    def make_head(wl, ncopies, fmt, bits, group, clip):
         w = synth.weight(wl.n, wl.k, wl.w_dtype, seed=wl.w_seed, device=dev)
         sdt = torch.float16 if wl.scale_dtype == synth.F16 else torch.bfloat16
-        wql.wql_quantize(w[:256], wl.bits, wl.group, sdt, wl.clip)   # load the kernel
+        wql.wql_quantize(w[:256], bits, group, sdt, clip, fmt=fmt)   # load the kernel
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        qw = wql.wql_quantize(w, wl.bits, wl.group, sdt, wl.clip)
+        qw = wql.wql_quantize(w, bits, group, sdt, clip, fmt=fmt)
         b.record(stream)
         torch.cuda.synchronize()
         qms = a.elapsed_time(b)
-        copies = [qw] + [wql.QuantizedWeight(qw.qweight.clone(), qw.scales.clone(), qw.bits,
-                                             qw.group, qw.n, qw.k) for _ in range(ncopies - 1)]
+        copies = [qw] + [wql.QuantizedWeight(
+            qw.qweight.clone(), qw.scales.clone(), qw.bits, qw.group, qw.n, qw.k, qw.fmt,
+            qw.zeros.clone() if qw.zeros is not None else None) for _ in range(ncopies - 1)]
         return w, copies, qms
 
-    def head_block(key, ncopies, topks, label):
+    def head_block(key, ncopies, topks, label, fmt=wql.FMT_SYM, bits=None, group=None,
+                   ms=None):
         wl = synth.WORKLOADS[key]
-        w, copies, qms = make_head(wl, ncopies)
+        bits = wl.bits if bits is None else bits
+        group = wl.group if group is None else group
+        clip = wl.clip if fmt == wql.FMT_SYM else wql.CLIP_RTN
+        w, copies, qms = make_head(wl, ncopies, fmt, bits, group, clip)
         del w
-        wbytes = copies[0].qweight.numel() * copies[0].qweight.element_size() + \
-            copies[0].scales.numel() * 2
-        blk = {"workload": key, "n": wl.n, "k": wl.k, "bits": wl.bits,
-               "group": wl.group or "row", "clip": "mse" if wl.clip else "rtn",
+        wbytes = copies[0].nbytes()
+        blk = {"workload": key, "n": wl.n, "k": wl.k, "bits": bits,
+               "group": group or "row", "clip": "mse" if clip else "rtn",
+               "format": {wql.FMT_SYM: "symmetric", wql.FMT_E4M3: "fp8 e4m3",
+                          wql.FMT_ASYM: "int4 with zero points"}[fmt],
                "weight_copies": ncopies, "weight_bytes": wbytes, "quantize_ms": round(qms, 2),
                "l2": label, "calls": {}}
-        for m in wl.ms:
+        for m in (wl.ms if ms is None else ms):
             x = synth.activations(m, wl.k, wl.x_dtype, seed=1000 + m, device=dev)
             for topk in topks(m):
-                blk["calls"][f"M{m}_top{topk}"] = entry(wl, m, topk, copies, x)
+                blk["calls"][f"M{m}_top{topk}"] = entry(wl, m, topk, copies, x, bits, group,
+                                                        wbytes)
         del copies
         torch.cuda.empty_cache()
         return blk
@@ -576,6 +584,10 @@ def run_configs(dev, stream, pk: dict, calls_per_sample: int = 12, samples: int 
     res["C3"] = head_block("qwen_151936x1024_w8g128", 2, lambda m: (0, 8), hbm)
     res["C5"] = head_block("head_248320x5120_w4g128_mse", 2,
                            lambda m: (0, 8) if m == 1 else (8,), hbm)
+    res["C5_fp8"] = head_block("head_248320x5120_w4g128_mse", 2, lambda m: (0, 8), hbm,
+                               fmt=wql.FMT_E4M3, bits=8, group=0, ms=(1, 16))
+    res["C2_asym"] = head_block("qwen_151936x1024_w4g64", 4, lambda m: (0, 8), hbm,
+                                fmt=wql.FMT_ASYM, bits=4, group=128, ms=(1, 16))
     res["C4"] = argmax_study(dev)
     res["clocks"] = clocks.stop()
     return res

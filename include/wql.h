@@ -65,7 +65,19 @@ typedef enum wql_clip {
   WQL_CLIP_MSE = 1   /* ratios 1.0, 0.95, 0.9, 0.85, 0.8; least squared error */
 } wql_clip;
 
-/* A quantised lm_head weight as produced by wql_quantize().
+/* Code format of a quantised weight (wql_weight.format). */
+typedef enum wql_format {
+  WQL_FMT_SYM = 0,   /* symmetric integers: int4 nibble = q + 8, or int8 q */
+  WQL_FMT_E4M3 = 1,  /* bits 8, group 0: fp8 e4m3 codes, one scale per row
+                        (radiance_lmhead_int4.py module docstring: the
+                        per-channel fp8 head it compares against) */
+  WQL_FMT_ASYM = 2   /* bits 4, group a multiple of 128: nibble = q in 0..15
+                        and a zero point z per group, w ~ (q - z) * s
+                        ("[CORE] Quantized lm-head Framework", the sym=False
+                        lm_head model of its lm-eval table) */
+} wql_format;
+
+/* A quantised lm_head weight as produced by wql_quantize() / wql_quantize_ex().
  *   bits 4: qweight is int32 [n, k/8]; word i of a row holds elements
  *           8i .. 8i+7, element 8i + j in the nibble at position
  *           p = 4*(j % 2) + j/2 (bits [4p, 4p + 4)): even elements fill bits
@@ -75,17 +87,24 @@ typedef enum wql_clip {
  *           mask per 16-bit half yields an adjacent element pair.)
  *   bits 8: qweight is int8 [n, k], two's complement q in [-127, 127].
  *   scales: [n, k / group] of scale_dtype, or [n, 1] when group == 0.
+ *   format WQL_FMT_E4M3 (bits 8, group 0): qweight is uint8 [n, k] e4m3
+ *           codes ("fn" variant: no infinities, 0x7F/0xFF NaN, largest
+ *           finite 448), w ~ e4m3(q) * s[row].
+ *   format WQL_FMT_ASYM (bits 4): qweight as for bits 4 with nibble = q in
+ *           0..15 (no bias), zeros uint8 [n, k / group], w ~ (q - z) * s.
  * Requirements: k % 64 == 0; group is 0 or a multiple of 64 dividing k;
  * qweight 16-byte aligned; scales 2-byte aligned; n < 2^31. */
 typedef struct wql_weight {
   int32_t bits;         /* 4 or 8 */
   int32_t group;        /* G (multiple of 64) or 0 = one scale per row */
   int32_t scale_dtype;  /* WQL_F16 or WQL_BF16 */
-  int32_t reserved;     /* must be 0 */
+  int32_t format;       /* wql_format; WQL_FMT_SYM (0) for the layouts above */
   int64_t n;            /* vocab rows */
   int64_t k;            /* hidden size */
   const void* qweight;  /* device */
   const void* scales;   /* device */
+  const void* zeros;    /* device uint8 [n, k / group] zero points 0..15
+                           (WQL_FMT_ASYM), else NULL */
 } wql_weight;
 
 /* Largest top-K width supported by wql_logits / wql_topk_rescore. */
@@ -109,6 +128,28 @@ wql_status wql_quantize(const void* w, int32_t w_dtype, int64_t n, int64_t k,
                         int32_t bits, int32_t group, int32_t scale_dtype,
                         int32_t clip, void* qweight_out, void* scales_out,
                         cudaStream_t stream);
+
+/* wql_quantize with a code format (wql_format):
+ *   WQL_FMT_SYM   exactly wql_quantize (zeros_out unused, may be NULL).
+ *   WQL_FMT_E4M3  bits 8, group 0, clip RTN.  Per row:
+ *                   s = RN_scale_dtype(max(fl32(amax) *f32 fl32(1/448), 1e-8f)),
+ *                   q = RN_e4m3(clamp(w /f32 s, -448, 448)) (ties to even),
+ *                 and q = 0 for the row when s rounds to zero.
+ *   WQL_FMT_ASYM  bits 4, group a multiple of 128 dividing k, clip RTN.  Per
+ *                 group, with lo = min(0, min w) and hi = max(0, max w):
+ *                   s = RN_scale_dtype(max((hi -f32 lo) *f32 fl32(1/15), 1e-8f)),
+ *                   z = clamp(rint_even(-lo /f32 s), 0, 15),
+ *                   q = clamp(rint_even(w /f32 s) + z, 0, 15),
+ *                 and q = z = 0 for the group when s rounds to zero;
+ *                 zeros_out device uint8 [n, k / group].
+ * (Neither page gives a formula for these two formats; these are the plain
+ * readings: amax maps to the largest finite e4m3, and plain asymmetric
+ * round-to-nearest with an integer zero point.)  Bit-exact with the
+ * definitions above. */
+wql_status wql_quantize_ex(const void* w, int32_t w_dtype, int64_t n, int64_t k,
+                           int32_t format, int32_t bits, int32_t group,
+                           int32_t scale_dtype, int32_t clip, void* qweight_out,
+                           void* scales_out, void* zeros_out, cudaStream_t stream);
 
 /* Pack nibbles (uint8 [n, k], values 0..15; higher bits are ignored) into the
  * int4 layout of wql_weight: packed_out int32 [n, k/8].  k % 8 == 0;

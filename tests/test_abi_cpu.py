@@ -54,8 +54,8 @@ def test_workspace_size_arithmetic():
     assert wql.wql_workspace_size(1, 10, wql.MAX_TOPK + 1) == 0
 
 
-def _weight(bits=4, group=64, sdt=1, n=1000, k=512, reserved=0, q=A, s=A):
-    return wql._WqlWeight(bits, group, sdt, reserved, n, k, q, s)
+def _weight(bits=4, group=64, sdt=1, n=1000, k=512, fmt=0, q=A, s=A, z=None):
+    return wql._WqlWeight(bits, group, sdt, fmt, n, k, q, s, z)
 
 
 def _logits(lib, w, x=A, xdt=1, m=2, bias=None, out=A, topk=0, idx=None, val=None, ws=None,
@@ -68,8 +68,9 @@ def test_logits_argument_checks(lib):
     before = wql.wql_launch_count()
     assert _logits(lib, None) == EINVAL
     assert _logits(lib, _weight(), m=-1) == EINVAL
-    assert _logits(lib, _weight(reserved=1)) == EINVAL
+    assert _logits(lib, _weight(fmt=7)) == EINVAL                # unknown format
     assert _logits(lib, _weight(), x=None) == EINVAL
+    assert _logits(lib, _weight(), out=None) == EINVAL           # no logits and no top-K
     assert _logits(lib, _weight(q=None)) == EINVAL
     assert _logits(lib, _weight(), topk=wql.MAX_TOPK + 1) == EINVAL
     assert _logits(lib, _weight(n=4), topk=5, idx=A, val=A) == EINVAL
@@ -83,6 +84,16 @@ def test_logits_argument_checks(lib):
     assert _logits(lib, _weight(), x=A + 2) == EUNSUPPORTED     # x not 16-byte aligned
     assert _logits(lib, _weight(q=A + 8)) == EUNSUPPORTED
     assert _logits(lib, _weight(), topk=8, idx=A, val=A) == EWORKSPACE
+    # candidates alone: logits_out NULL with top-K on passes the checks
+    assert _logits(lib, _weight(), out=None, topk=8, idx=A, val=A) == EWORKSPACE
+    # fp8 e4m3: bits 8 with one scale per row only
+    assert _logits(lib, _weight(fmt=1, bits=4, group=0)) == EUNSUPPORTED
+    assert _logits(lib, _weight(fmt=1, bits=8, group=64)) == EUNSUPPORTED
+    # zero points: int4, a group that is a multiple of 128, a zero-point table
+    assert _logits(lib, _weight(fmt=2, group=128)) == EINVAL          # no zeros
+    assert _logits(lib, _weight(fmt=2, group=64, z=A)) == EUNSUPPORTED
+    assert _logits(lib, _weight(fmt=2, bits=8, group=128, z=A)) == EUNSUPPORTED
+    assert _logits(lib, _weight(fmt=2, group=0, z=A)) == EUNSUPPORTED
     need = wql.wql_workspace_size(2, 1000, 8)
     assert _logits(lib, _weight(), topk=8, idx=A, val=A, ws=A, wsb=need - 1) == EWORKSPACE
     assert _logits(lib, _weight(), m=0) == OK                    # empty: nothing launched
@@ -100,6 +111,15 @@ def test_quantize_pack_rescore_argument_checks(lib):
     assert q(A, 0, 10, 512, 4, 64, 0, 0, A, A, None) == EUNSUPPORTED  # fp32 scales
     assert q(A, 0, 10, 500, 4, 64, 1, 0, A, A, None) == EUNSUPPORTED
     assert q(A, 0, 0, 512, 4, 64, 1, 0, A, A, None) == OK
+    qx = lib.wql_quantize_ex
+    assert qx(A, 0, 10, 512, 7, 4, 64, 1, 0, A, A, None, None) == EINVAL          # format
+    assert qx(A, 0, 10, 512, 1, 8, 64, 1, 0, A, A, None, None) == EUNSUPPORTED    # e4m3 group
+    assert qx(A, 0, 10, 512, 1, 8, 0, 1, 1, A, A, None, None) == EUNSUPPORTED     # e4m3 MSE
+    assert qx(A, 0, 10, 512, 1, 4, 0, 1, 0, A, A, None, None) == EUNSUPPORTED     # e4m3 bits
+    assert qx(A, 0, 10, 512, 2, 4, 128, 1, 0, A, A, None, None) == EINVAL         # no zeros
+    assert qx(A, 0, 10, 512, 2, 4, 64, 1, 0, A, A, A, None) == EUNSUPPORTED       # group 64
+    assert qx(A, 0, 10, 512, 2, 8, 128, 1, 0, A, A, A, None) == EUNSUPPORTED      # bits 8
+    assert qx(A, 0, 0, 512, 2, 4, 128, 1, 0, A, A, A, None) == OK
     assert lib.wql_pack(A, 4, 12, A, None) == EUNSUPPORTED
     assert lib.wql_pack(None, 4, 16, A, None) == EINVAL
     assert lib.wql_unpack(A, 0, 16, A, None) == OK
@@ -120,7 +140,8 @@ def test_embed_gather_argument_checks(lib):
 
     assert call(None) == EINVAL
     assert call(_weight(), t=-1) == EINVAL
-    assert call(_weight(reserved=1)) == EINVAL
+    assert call(_weight(fmt=7)) == EINVAL
+    assert call(_weight(fmt=1, bits=8, group=0)) == EUNSUPPORTED  # fp8 rows: not gathered
     assert call(_weight(), ids=None) == EINVAL
     assert call(_weight(), out=None) == EINVAL
     assert call(_weight(s=None)) == EINVAL

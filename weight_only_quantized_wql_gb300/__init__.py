@@ -7,11 +7,11 @@ There is no CPU or PyTorch fallback: if the library cannot be loaded, or a
 tensor is not on a CUDA device, the call raises.
 
 Functions
-  wql_quantize(w, bits, group, scale_dtype, clip)   -> QuantizedWeight
+  wql_quantize(w, bits, group, scale_dtype, clip, fmt=FMT_SYM) -> QuantizedWeight
   wql_pack(nibbles) / wql_unpack(packed, k)
   wql_workspace_size(m, n, topk)                    -> bytes
-  wql_logits(x, qw, bias=None, topk=0, workspace=None, out=None)
-                                                    -> (logits, topk_idx, topk_val)
+  wql_logits(x, qw, bias=None, topk=0, workspace=None, out=None,
+             candidates_only=False)             -> (logits, topk_idx, topk_val)
   wql_topk_rescore(x, w_ref, topk_idx, topk_val, logits, bias=None)
   wql_embed_gather(ids, qw, out_dtype=torch.float16, out=None) -> [*ids.shape, k]
   wql_status_string, wql_last_error, wql_launch_count
@@ -32,11 +32,13 @@ __all__ = [
     "wql_unpack", "wql_workspace_size", "wql_logits", "wql_logits_noalloc", "wql_topk_rescore",
     "wql_embed_gather",
     "wql_status_string", "wql_last_error", "wql_launch_count", "F32", "F16", "BF16",
-    "CLIP_RTN", "CLIP_MSE", "MAX_TOPK", "NOALLOC_SCRATCH_BYTES",
+    "CLIP_RTN", "CLIP_MSE", "MAX_TOPK", "NOALLOC_SCRATCH_BYTES", "FMT_SYM", "FMT_E4M3",
+    "FMT_ASYM",
 ]
 
 F32, F16, BF16 = 0, 1, 2
 CLIP_RTN, CLIP_MSE = 0, 1
+FMT_SYM, FMT_E4M3, FMT_ASYM = 0, 1, 2    # wql_format
 MAX_TOPK = 16
 MAX_CTAS = 1024
 _DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
@@ -61,9 +63,10 @@ class WQLError(RuntimeError):
 
 class _WqlWeight(ctypes.Structure):
     _fields_ = [("bits", ctypes.c_int32), ("group", ctypes.c_int32),
-                ("scale_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("scale_dtype", ctypes.c_int32), ("format", ctypes.c_int32),
                 ("n", ctypes.c_int64), ("k", ctypes.c_int64),
-                ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+                ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zeros", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -85,6 +88,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         i32, i64, vp, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
         lib.wql_quantize.restype = i32
         lib.wql_quantize.argtypes = [vp, i32, i64, i64, i32, i32, i32, i32, vp, vp, vp]
+        lib.wql_quantize_ex.restype = i32
+        lib.wql_quantize_ex.argtypes = [vp, i32, i64, i64, i32, i32, i32, i32, i32, vp, vp, vp,
+                                        vp]
         lib.wql_pack.restype = i32
         lib.wql_pack.argtypes = [vp, i64, i64, vp, vp]
         lib.wql_unpack.restype = i32
@@ -143,12 +149,14 @@ def _stream(device) -> ctypes.c_void_p:
 @dataclass
 class QuantizedWeight:
     """Packed weight + scale table, in the layout wql.h documents."""
-    qweight: torch.Tensor      # int32 [n, k/8] (bits 4) or int8 [n, k] (bits 8)
+    qweight: torch.Tensor      # int32 [n, k/8] (bits 4), int8 / uint8 e4m3 [n, k] (bits 8)
     scales: torch.Tensor       # fp16/bf16 [n, k/group] (or [n, 1])
     bits: int
     group: int                 # 0 = one scale per row
     n: int
     k: int
+    fmt: int = FMT_SYM         # wql_format
+    zeros: torch.Tensor | None = None   # uint8 [n, k/group] zero points (FMT_ASYM)
 
     @property
     def scale_dtype(self) -> int:
@@ -156,18 +164,20 @@ class QuantizedWeight:
 
     def _struct(self) -> _WqlWeight:
         # built once per (qweight, scales) storage; calls reuse it
+        zp = self.zeros.data_ptr() if self.zeros is not None else None
         key = (self.qweight.data_ptr(), self.scales.data_ptr(), self.bits, self.group,
-               self.n, self.k, self.scales.dtype)
+               self.n, self.k, self.scales.dtype, self.fmt, zp)
         cached = self.__dict__.get("_st")
         if cached is None or cached[0] != key:
-            cached = (key, _WqlWeight(self.bits, self.group, self.scale_dtype, 0, self.n,
-                                      self.k, key[0], key[1]))
+            cached = (key, _WqlWeight(self.bits, self.group, self.scale_dtype, self.fmt,
+                                      self.n, self.k, key[0], key[1], zp))
             self.__dict__["_st"] = cached
         return cached[1]
 
     def nbytes(self) -> int:
+        z = self.zeros.numel() if self.zeros is not None else 0
         return self.qweight.numel() * self.qweight.element_size() + \
-            self.scales.numel() * self.scales.element_size()
+            self.scales.numel() * self.scales.element_size() + z
 
 
 class Workspace:
@@ -217,21 +227,27 @@ def wql_workspace_size(m: int, n: int, topk: int) -> int:
 
 
 def wql_quantize(w: torch.Tensor, bits: int, group: int, scale_dtype=torch.float16,
-                 clip: int = CLIP_RTN) -> QuantizedWeight:
-    """Quantise + pack a [n, k] fp32/fp16/bf16 CUDA weight (see wql.h)."""
+                 clip: int = CLIP_RTN, fmt: int = FMT_SYM) -> QuantizedWeight:
+    """Quantise + pack a [n, k] fp32/fp16/bf16 CUDA weight (see wql.h;
+    fmt FMT_E4M3 / FMT_ASYM go through wql_quantize_ex)."""
     lib = load()
     _cuda(w, "w")
     n, k = w.shape
     g = k if group == 0 else group
     if bits == 4:
         qw = torch.empty((n, k // 8), dtype=torch.int32, device=w.device)
+    elif fmt == FMT_E4M3:
+        qw = torch.empty((n, k), dtype=torch.uint8, device=w.device)
     else:
         qw = torch.empty((n, k), dtype=torch.int8, device=w.device)
     sc = torch.empty((n, k // g if g else 0), dtype=scale_dtype, device=w.device)
-    _check("wql_quantize", lib.wql_quantize(_ptr(w), _DTYPE_CODE[w.dtype], n, k, bits, group,
-                                            _DTYPE_CODE[scale_dtype], clip, _ptr(qw),
-                                            _ptr(sc), _stream(w.device)))
-    return QuantizedWeight(qw, sc, bits, group, n, k)
+    zeros = None
+    if fmt == FMT_ASYM:
+        zeros = torch.empty((n, k // g if g else 0), dtype=torch.uint8, device=w.device)
+    _check("wql_quantize_ex", lib.wql_quantize_ex(
+        _ptr(w), _DTYPE_CODE[w.dtype], n, k, fmt, bits, group, _DTYPE_CODE[scale_dtype], clip,
+        _ptr(qw), _ptr(sc), _ptr(zeros), _stream(w.device)))
+    return QuantizedWeight(qw, sc, bits, group, n, k, fmt, zeros)
 
 
 def wql_pack(nibbles: torch.Tensor) -> torch.Tensor:
@@ -260,17 +276,21 @@ def default_workspace(device=None) -> Workspace:
 def wql_logits(x: torch.Tensor, qw: QuantizedWeight, bias: torch.Tensor | None = None,
                topk: int = 0, workspace: Workspace | None = None,
                out: torch.Tensor | None = None, topk_idx: torch.Tensor | None = None,
-               topk_val: torch.Tensor | None = None):
+               topk_val: torch.Tensor | None = None, candidates_only: bool = False):
     """logits [m, n] (x.dtype), and top-K (idx int32, val fp32) when topk > 0.
 
     x of any leading shape is flattened to [m, k] (radiance_lmhead_int4.py,
-    apply()); the logits are returned with x's leading shape."""
+    apply()); the logits are returned with x's leading shape.  With
+    candidates_only (topk > 0) no logits are written (logits_out NULL) and
+    None is returned in their place."""
     lib = load()
     lead = x.shape[:-1]
     x2 = x.reshape(-1, x.shape[-1])
     _cuda(x2, "x")
     m = x2.shape[0]
-    if out is None:
+    if candidates_only and topk <= 0:
+        raise ValueError("candidates_only needs topk > 0")
+    if out is None and not candidates_only:
         out = torch.empty((m, qw.n), dtype=x.dtype, device=x.device)
     if topk > 0:
         if topk_idx is None:
@@ -286,7 +306,7 @@ def wql_logits(x: torch.Tensor, qw: QuantizedWeight, bias: torch.Tensor | None =
         _ptr(x2), _DTYPE_CODE[x.dtype], m, ctypes.byref(st), _ptr(bias), _ptr(out), topk,
         _ptr(topk_idx) if topk > 0 else None, _ptr(topk_val) if topk > 0 else None,
         _ptr(ws), ws.numel(), _stream(x.device)))
-    logits = out.reshape(*lead, qw.n)
+    logits = out.reshape(*lead, qw.n) if out is not None else None
     if topk > 0:
         return logits, topk_idx.reshape(*lead, topk), topk_val.reshape(*lead, topk)
     return logits, None, None

@@ -20,7 +20,7 @@ struct Plan {
   int nt;            // 8-column MMA n-tiles
   int warps;         // warps per CTA
   int cap;           // candidate buffer entries per (warp, token)
-  int step_cols, s_real, s, corr_pitch, corr_floats, nunits;
+  int step_cols, s_real, s, corr_pitch, corr_floats, nunits, xsum_off;
   uint32_t xpitch;
   uint32_t off_x, off_zero, off_corr, off_ring, off_list, off_cnt, off_misc, off_ugrp;
   size_t smem;
@@ -31,7 +31,7 @@ struct Plan {
 // (reused at the end for the slots of tiles cut between warps and for the
 // top-K survivors), (top-K) the warps' candidate buffers, counts and
 // thresholds, the small words and head stashes, and the unit -> group table.
-Plan plan(int m, int k, int bits, int group, int topk, int cap) {
+Plan plan(int m, int k, int bits, int group, int topk, int format, int cap) {
   Plan P{};
   P.gw2 = bits == 4 && (group % 128) != 0;
   P.step_cols = bits == 4 ? 128 : 64;
@@ -44,6 +44,9 @@ Plan plan(int m, int k, int bits, int group, int topk, int cap) {
   P.xpitch = (uint32_t)P.s_real * (uint32_t)P.step_cols * 2u;
   P.corr_pitch = 2 * P.s_real;
   P.corr_floats = P.gw2 ? kMaxTok * P.corr_pitch : P.s_real * kMaxTok;
+  // zero points: the plain sums of x per step follow the offset sums
+  P.xsum_off = P.corr_floats;
+  if (format == WQL_FMT_ASYM) P.corr_floats *= 2;
   P.nunits = bits == 4 ? 2 * P.s_real : P.s_real;
   const bool tk = topk > 0;
   uint32_t off = 0;
@@ -70,10 +73,10 @@ Plan plan(int m, int k, int bits, int group, int topk, int cap) {
 // Candidate buffers of 32 entries per (warp, token) (fewer compactions),
 // else of K + 16 (the least the appends of one tile need after a compaction)
 // when the larger ones do not fit.
-Plan plan(int m, int k, int bits, int group, int topk) {
-  const Plan P = plan(m, k, bits, group, topk, 32);
+Plan plan(int m, int k, int bits, int group, int topk, int format) {
+  const Plan P = plan(m, k, bits, group, topk, format, 32);
   if (P.smem <= kSmemLimit || topk <= 0) return P;
-  return plan(m, k, bits, group, topk, topk + 16);
+  return plan(m, k, bits, group, topk, format, topk + 16);
 }
 
 }  // namespace
@@ -93,20 +96,22 @@ extern template cudaError_t dispatch_xs<__nv_bfloat16, __nv_bfloat16>(const Deco
                                                                       cudaStream_t);
 }  // namespace decode_detail
 
-size_t decode_smem_bytes(int m, int k, int bits, int group_eff, int topk) {
-  return plan(m, k, bits, group_eff, topk).smem;
+size_t decode_smem_bytes(int m, int k, int bits, int group_eff, int topk, int format) {
+  return plan(m, k, bits, group_eff, topk, format).smem;
 }
 
-int decode_max_tokens(int k, int bits, int group_eff, int topk) {
+int decode_max_tokens(int k, int bits, int group_eff, int topk, int format) {
   for (int m = kMaxTok; m >= 1; --m)
-    if (plan(m, k, bits, group_eff, topk).smem <= kSmemLimit) return m;
+    if (plan(m, k, bits, group_eff, topk, format).smem <= kSmemLimit) return m;
   return 0;
 }
 
 cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s) {
   (void)err;   // the decode kernel has no waits that can time out
   if (a.m < 1 || a.m > kMaxTok) return cudaErrorInvalidConfiguration;
-  const Plan P = plan(a.m, a.k, a.bits, a.group_eff, a.topk);
+  const Plan P = plan(a.m, a.k, a.bits, a.group_eff, a.topk, a.format);
+  if (a.format == WQL_FMT_ASYM && (P.gw2 || a.zeros == nullptr))
+    return cudaErrorInvalidConfiguration;
   if (P.smem > kSmemLimit) return cudaErrorInvalidConfiguration;
   if (a.topk > 0 && (a.counter == nullptr || a.cand == nullptr))
     return cudaErrorInvalidConfiguration;
@@ -130,6 +135,9 @@ cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s
   p.off_cnt = P.off_cnt;
   p.off_misc = P.off_misc;
   p.cap = P.cap;
+  p.asym = a.format == WQL_FMT_ASYM ? 1 : 0;
+  p.xsum_off = P.xsum_off;
+  p.corr_floats = P.corr_floats;
   // linear scale addressing: with two group halves per step, groups of 64
   // columns, no half step at a row's end and 4-byte aligned scale rows (one
   // 32-bit load per row); otherwise one group per step

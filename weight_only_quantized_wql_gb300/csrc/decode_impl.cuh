@@ -95,6 +95,9 @@ struct DecodeParams {
   uint32_t xpitch;   // bytes per token row of x in shared memory
   uint32_t off_x, off_zero, off_corr, off_ring, off_list, off_cnt, off_misc, off_ugrp;
   int early_weights;  // 1: weights may be read before the preceding kernel ends
+  int asym;           // int4 codes with a zero point per group (no half steps)
+  int xsum_off;       // floats from the offset sums to the plain sums of x (asym)
+  int corr_floats;    // floats of both (cleared at launch)
 };
 
 __host__ __device__ constexpr uint32_t round_up_u32(uint32_t v, uint32_t a) {
@@ -121,6 +124,11 @@ __device__ __forceinline__ uint32_t ldg_scale(const uint16_t* p) {
   asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
   return (uint32_t)v;
 }
+__device__ __forceinline__ uint32_t ldg_u8(const uint8_t* p) {
+  uint16_t v;
+  asm("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return (uint32_t)v;
+}
 __device__ __forceinline__ uint32_t ldg_scale2(const uint16_t* p) {
   uint32_t v;
   asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -136,15 +144,20 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // Code conversion per variant: fp16 int4 reads the high nibble of each byte
 // in place (x pre-scaled by 1/16 there); everything else uses OffsetCodes.
-template <int BITS, typename XT>
+template <int BITS, typename XT, bool F8>
 struct CodesOf {
   using type = OffsetCodes<BITS, XT>;
   static constexpr bool kScaledX = false;
 };
 template <>
-struct CodesOf<4, __half> {
+struct CodesOf<4, __half, false> {
   using type = Int4F16Scaled;
   static constexpr bool kScaledX = true;
+};
+template <typename XT>
+struct CodesOf<8, XT, true> {   // fp8 e4m3 codes: exact values, no offset
+  using type = E4M3Codes<XT>;
+  static constexpr bool kScaledX = false;
 };
 
 // The value the MMA adds per code on top of x*q, per activation element:
@@ -157,11 +170,23 @@ __device__ __forceinline__ float offset_sum(const uint4& v) {
   for (int q = 0; q < 4; ++q) {
     const float e0 = scale_bits_to_f32<XT>((uint16_t)(w[q] & 0xFFFFu));
     const float e1 = scale_bits_to_f32<XT>((uint16_t)(w[q] >> 16));
-    if (CodesOf<BITS, XT>::kScaledX && (q & 1)) hi += e0 + e1;
+    if (CodesOf<BITS, XT, false>::kScaledX && (q & 1)) hi += e0 + e1;
     else lo += e0 + e1;
   }
-  if constexpr (CodesOf<BITS, XT>::kScaledX) return 1032.0f * lo + 1152.0f * hi;
+  if constexpr (CodesOf<BITS, XT, false>::kScaledX) return 1032.0f * lo + 1152.0f * hi;
   else return OffsetCodes<BITS, XT>::kOffset * lo;
+}
+
+// The plain sum of one 16-byte piece of x (eight elements).
+template <typename XT>
+__device__ __forceinline__ float piece_sum(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float r = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    r += scale_bits_to_f32<XT>((uint16_t)(w[q] & 0xFFFFu)) +
+         scale_bits_to_f32<XT>((uint16_t)(w[q] >> 16));
+  return r;
 }
 
 // Swizzle of x's 16-byte pieces inside each aligned run of 8 (by token).
@@ -347,17 +372,19 @@ __device__ __forceinline__ void compact(const Cands& C, int tk, int K) {
 // halves, groups of 64 columns with the two halves' entries adjacent and
 // 4-byte aligned (one 32-bit load); otherwise one group per step.  Without
 // LIN they are looked up per step in a unit -> group table.
-template <int BITS, bool GW2, bool LIN, typename XT, typename ST, int NT>
+template <int BITS, bool GW2, bool LIN, typename XT, typename ST, int NT, bool F8>
 __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
-  using Codes = typename CodesOf<BITS, XT>::type;
+  using Codes = typename CodesOf<BITS, XT, F8>::type;
   constexpr int W = warps_of(NT);
   constexpr int kThr = W * 32;
-  constexpr bool kScaledX = CodesOf<BITS, XT>::kScaledX;
+  constexpr bool kScaledX = CodesOf<BITS, XT, F8>::kScaledX;
   constexpr int kStepCols = BITS == 4 ? 128 : 64;       // columns per step
   constexpr int kLanePieces = kStepCols / 32;           // 16-byte x pieces per lane per step
   constexpr uint32_t kXStepBytes = kStepCols * 2;       // x bytes per step
-  constexpr bool kHasOffset = !(BITS == 8 && std::is_same<XT, __nv_bfloat16>::value);
+  constexpr bool kHasOffset = !F8 && !(BITS == 8 && std::is_same<XT, __nv_bfloat16>::value);
+  // zero points: int4 with one group per step only (the host enforces it)
+  constexpr bool kMayAsym = BITS == 4 && !GW2;
 
   extern __shared__ __align__(128) uint8_t sm[];
   const LogitsArgs& a = p.a;
@@ -459,13 +486,14 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
           SA |= ldg_scale(rp.spa + h1) << 16;
           SB |= ldg_scale(rp.spb + h1) << 16;
         }
-      } else if constexpr (LIN) {   // one group per step
-        SA = ldg_scale(rp.spa + j);
-        SB = ldg_scale(rp.spb + j);
-      } else {
-        const int gi = ugrp[BITS == 4 ? 2 * s : s];
+      } else {                      // one group per step
+        const int gi = LIN ? j : ugrp[BITS == 4 ? 2 * s : s];
         SA = ldg_scale(rp.spa + gi);
         SB = ldg_scale(rp.spb + gi);
+        if (kMayAsym && p.asym) {   // the zero points ride in the upper halves
+          SA |= ldg_u8(a.zeros + (rp.spa - scales) + gi) << 16;
+          SB |= ldg_u8(a.zeros + (rp.spb - scales) + gi) << 16;
+        }
       }
     }
   };
@@ -477,12 +505,11 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
   unsigned int* flag = reinterpret_cast<unsigned int*>(sm + p.off_misc + kMaxWarps * 4);
   unsigned long long* cbuf = reinterpret_cast<unsigned long long*>(sm + p.off_list);
   unsigned int* ccnt = reinterpret_cast<unsigned int*>(sm + p.off_cnt);      // [2][W][m]
-  const int nunits_c = GW2 ? p.corr_pitch : p.S_real;    // offset-sum units per token
 
   // This CTA's own shared memory is cleared before the wait for the
   // preceding kernel: the offset sums (entries of tokens past m stay 0), the
   // zero region, the candidate counts and thresholds.
-  for (int i = threadIdx.x; i < kMaxTok * nunits_c; i += kThr) corr[i] = 0.f;
+  for (int i = threadIdx.x; i < p.corr_floats; i += kThr) corr[i] = 0.f;
   for (int i = threadIdx.x; i < kZeroBytes / 16; i += kThr)
     *reinterpret_cast<uint4*>(sm + p.off_zero + i * 16) = make_uint4(0u, 0u, 0u, 0u);
   if (K > 0)
@@ -529,6 +556,9 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
         if (i < total && pc[b] < kp)
           v[b] = *reinterpret_cast<const uint4*>(xg + (size_t)tk[b] * k + pc[b] * 8);
       }
+      float xplain[kB];   // plain sums of the pieces (zero points)
+#pragma unroll
+      for (int b = 0; b < kB; ++b) xplain[b] = kMayAsym && p.asym ? piece_sum<XT>(v[b]) : 0.f;
 #pragma unroll
       for (int b = 0; b < kB; ++b) {
         if (i0 + b * kThr >= total) continue;
@@ -539,6 +569,8 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
         const uint32_t q = (uint32_t)pc[b];
         const uint32_t phys = (q & ~7u) | ((q ^ x_swz<GW2>(tk[b])) & 7u);
         *reinterpret_cast<uint4*>(xs + (size_t)tk[b] * p.xpitch + phys * 16) = v[b];
+        if (kMayAsym && p.asym && pc[b] < kp)
+          atomicAdd(&corr[p.xsum_off + (pc[b] / (kStepCols / 8)) * kMaxTok + tk[b]], xplain[b]);
         if (kHasOffset && pc[b] < kp) {
           const float o = offset_sum<BITS, XT>(v[b]);
           if constexpr (GW2) atomicAdd(&corr[tk[b] * p.corr_pitch + (pc[b] >> 3)], -o);
@@ -627,7 +659,7 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
         if (row < n && tok < m) {
           float val = v[nt][c];
           if (bias) val += to_f32(bias[row]);
-          logits[(size_t)tok * n + row] = from_f32<XT>(val);
+          if (logits) logits[(size_t)tok * n + row] = from_f32<XT>(val);
           if (K > 0) {
             key[nt][c] = topk_key(val, (uint32_t)row);
             pass[nt][c] = (uint32_t)(key[nt][c] >> 32) >= thr[nt][c & 1];
@@ -744,6 +776,18 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
     } else {
       const float fa = scale_bits_to_f32<ST>((uint16_t)scA);
       const float fb = scale_bits_to_f32<ST>((uint16_t)scB);
+      if (kMayAsym && p.asym) {
+        // zero points: sum x*(u - z) = sum x*(u - 8) + (8 - z) * sum x
+        const float da = 8.0f - (float)(scA >> 16), db = 8.0f - (float)(scB >> 16);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float2 sx = *reinterpret_cast<const float2*>(cq[nt] + p.xsum_off + j * kMaxTok);
+          p0[nt][0] = fmaf(da, sx.x, p0[nt][0]);
+          p0[nt][1] = fmaf(da, sx.y, p0[nt][1]);
+          p0[nt][2] = fmaf(db, sx.x, p0[nt][2]);
+          p0[nt][3] = fmaf(db, sx.y, p0[nt][3]);
+        }
+      }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         acc[nt][0] = fmaf(fa, p0[nt][0] + p1[nt][0], acc[nt][0]);
@@ -952,9 +996,9 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
   if (threadIdx.x == 0) *a.counter = 0u;
 }
 
-template <int BITS, bool GW2, bool LIN, typename XT, typename ST, int NT>
+template <int BITS, bool GW2, bool LIN, typename XT, typename ST, int NT, bool F8 = false>
 cudaError_t launch_t(const DecodeParams& p, size_t smem, int ctas, cudaStream_t s) {
-  auto kern = decode_kernel<BITS, GW2, LIN, XT, ST, NT>;
+  auto kern = decode_kernel<BITS, GW2, LIN, XT, ST, NT, F8>;
   // per instantiation: raise the dynamic smem limit when a launch needs more,
   // and ask for the smallest shared-memory carveout that holds it, leaving
   // the rest of the SM's 256 KB to L1 (scale rows are read through L1)
@@ -999,6 +1043,10 @@ cudaError_t dispatch_lin(const DecodeParams& p, bool gw2, int nt, size_t smem, i
   if (p.a.bits == 4) {
     if (nt == 1) return launch_t<4, false, LIN, XT, ST, 1>(p, smem, ctas, s);
     return launch_t<4, false, LIN, XT, ST, 2>(p, smem, ctas, s);
+  }
+  if (p.a.format == WQL_FMT_E4M3) {
+    if (nt == 1) return launch_t<8, false, LIN, XT, ST, 1, true>(p, smem, ctas, s);
+    return launch_t<8, false, LIN, XT, ST, 2, true>(p, smem, ctas, s);
   }
   if (nt == 1) return launch_t<8, false, LIN, XT, ST, 1>(p, smem, ctas, s);
   return launch_t<8, false, LIN, XT, ST, 2>(p, smem, ctas, s);

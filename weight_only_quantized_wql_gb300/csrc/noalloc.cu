@@ -114,8 +114,6 @@ cudaError_t area_on_current_device(void** out) {
   return cudaSuccess;
 }
 
-bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-bool is_half(int d) { return d == WQL_F16 || d == WQL_BF16; }
 
 }  // namespace
 }  // namespace wql
@@ -127,26 +125,13 @@ extern "C" wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t
                                          void* logits_out, int32_t topk, int32_t* topk_idx,
                                          float* topk_val, cudaStream_t stream) {
   // Host checks first: a rejected call makes no CUDA call at all.
-  if (!w || m < 0 || w->n < 0 || w->k <= 0 || w->group < 0 || w->reserved != 0)
-    return WQL_EINVAL;
-  if (topk < 0 || topk > WQL_MAX_TOPK) return WQL_EINVAL;
+  int64_t g = 0;
+  const wql_status st = check_logits_args(x, x_dtype, m, w, bias, logits_out, topk, topk_idx,
+                                          topk_val, &g);
+  if (st != WQL_OK) return st;
   const int64_t n = w->n, k = w->k;
-  if (m > 0 && n > 0) {
-    if (!x || !w->qweight || !w->scales || !logits_out) return WQL_EINVAL;
-    if (topk > 0 && (!topk_idx || !topk_val)) return WQL_EINVAL;
-    if (topk > n) return WQL_EINVAL;
-  }
-  if (w->bits != 4 && w->bits != 8) return WQL_EUNSUPPORTED;
-  if (!is_half(x_dtype) || !is_half(w->scale_dtype)) return WQL_EUNSUPPORTED;
-  const int64_t g = w->group == 0 ? k : w->group;
-  if (k % 64 != 0 || g % 64 != 0 || k % g != 0) return WQL_EUNSUPPORTED;
-  if (n >= (int64_t(1) << 31) || m >= (int64_t(1) << 31) || k >= (int64_t(1) << 30))
-    return WQL_EUNSUPPORTED;
-  if (!is_aligned(x, 16) || !is_aligned(w->qweight, 16) || !is_aligned(w->scales, 2) ||
-      !is_aligned(logits_out, 2) || !is_aligned(bias, 2))
-    return WQL_EUNSUPPORTED;
   if (m == 0 || n == 0) return WQL_OK;
-  const int slice_tokens = decode_max_tokens((int)k, w->bits, (int)g, topk);
+  const int slice_tokens = decode_max_tokens((int)k, w->bits, (int)g, topk, w->format);
   if (slice_tokens < 1) return WQL_EUNSUPPORTED;
   const int64_t slice_max = m < slice_tokens ? m : slice_tokens;
   // Every slice reuses the same area, so one slice's layout is the need.
@@ -175,6 +160,8 @@ extern "C" wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t
   base.k = (int)k;
   base.bias = bias;
   base.topk = topk;
+  base.format = w->format;
+  base.zeros = static_cast<const uint8_t*>(w->zeros);
   base.counter = counter;   // also schedules the decode kernel's work units
   if (topk > 0) {
     base.cand = reinterpret_cast<unsigned long long*>(ws + lay.cand_off);
@@ -185,7 +172,8 @@ extern "C" wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t
     LogitsArgs a = base;
     a.x = static_cast<const unsigned char*>(x) + (size_t)m0 * (size_t)k * esz;
     a.m = (int)mc;
-    a.logits = static_cast<unsigned char*>(logits_out) + (size_t)m0 * (size_t)n * esz;
+    a.logits = logits_out ? static_cast<unsigned char*>(logits_out) + (size_t)m0 * (size_t)n * esz
+                          : nullptr;
     if (topk > 0) {
       a.topk_idx = topk_idx + (size_t)m0 * topk;
       a.topk_val = topk_val + (size_t)m0 * topk;

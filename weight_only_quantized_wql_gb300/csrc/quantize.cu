@@ -10,9 +10,11 @@
 // the strictly smallest error.  Every operation is the IEEE operation the
 // definition names, so the result is bit-exact on any conforming machine.
 // The weight is streamed from global memory (L1-cached re-reads); no fp32
-// copy of the matrix is made.
+// copy of the matrix is made.  The fp8 e4m3 per-row and the zero-point int4
+// formats (wql_quantize_ex) follow their own definitions below.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "wql_common.cuh"
 
@@ -34,6 +36,71 @@ __device__ __forceinline__ int code_of(float w, float s, int qmin, int qmax) {
   return (int)r;
 }
 
+// fp8 e4m3 codes of one row (WQL_FMT_E4M3): s = RN(max(amax * fl32(1/448),
+// 1e-8)), q = RN_e4m3(clamp(w / s, -448, 448)) with ties to even (the
+// conversion's own rounding; the clamp keeps NaN, which converts to NaN).
+template <typename WT>
+__device__ void quantize_e4m3_row(const QuantizeArgs& a, const WT* w, int64_t gid) {
+  const int G = a.group_eff;
+  float amax = 0.0f;
+  for (int j = 0; j < G; ++j) amax = fmaxf(amax, fabsf(load_w(w, j)));
+  float prod = __fmul_rn(amax, a.ratio_c[0]);
+  prod = prod < 1e-8f ? 1e-8f : prod;
+  const uint16_t sbits = round_scale(prod, a.scale_dtype);
+  const float s = scale_to_f32(sbits, a.scale_dtype);
+  a.scales[gid] = sbits;
+  uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(a.qweight) + gid * (int64_t)G);
+  for (int j4 = 0; j4 < G; j4 += 4) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t c = 0;
+      if (s != 0.0f) {
+        float t = __fdiv_rn(load_w(w, j4 + j), s);
+        if (t > 448.0f) t = 448.0f;
+        if (t < -448.0f) t = -448.0f;
+        c = (uint32_t)__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+      }
+      word |= c << (8 * j);
+    }
+    out[j4 / 4] = word;
+  }
+}
+
+// Zero-point int4 codes of one group (WQL_FMT_ASYM): with lo = min(0, w)
+// and hi = max(0, w), s = RN(max((hi - lo) * fl32(1/15), 1e-8)),
+// z = clamp(rint(-lo / s), 0, 15), q = clamp(rint(w / s) + z, 0, 15).
+template <typename WT>
+__device__ void quantize_asym_group(const QuantizeArgs& a, const WT* w, int64_t row, int64_t gi,
+                                    int64_t gid) {
+  const int G = a.group_eff;
+  float lo = 0.0f, hi = 0.0f;
+  for (int j = 0; j < G; ++j) {
+    const float v = load_w(w, j);
+    if (v < lo) lo = v;
+    if (v > hi) hi = v;
+  }
+  float prod = __fmul_rn(__fsub_rn(hi, lo), a.ratio_c[0]);
+  prod = prod < 1e-8f ? 1e-8f : prod;
+  const uint16_t sbits = round_scale(prod, a.scale_dtype);
+  const float s = scale_to_f32(sbits, a.scale_dtype);
+  a.scales[gid] = sbits;
+  int z = 0;
+  if (s != 0.0f) z = min(max((int)rintf(__fdiv_rn(-lo, s)), 0), 15);
+  a.zeros[gid] = (uint8_t)z;
+  uint32_t* out = reinterpret_cast<uint32_t*>(a.qweight) + (row * a.k + gi * (int64_t)G) / 8;
+  for (int j8 = 0; j8 < G; j8 += 8) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      int q = 0;
+      if (s != 0.0f) q = min(max((int)rintf(__fdiv_rn(load_w(w, j8 + j), s)) + z, 0), 15);
+      word |= (uint32_t)q << (4 * nibble_pos(j));
+    }
+    out[j8 / 8] = word;
+  }
+}
+
 template <typename WT>
 __global__ void __launch_bounds__(128) quantize_kernel(const QuantizeArgs a) {
   const int64_t ngroups = a.k / a.group_eff;
@@ -43,6 +110,14 @@ __global__ void __launch_bounds__(128) quantize_kernel(const QuantizeArgs a) {
   const int64_t gi = gid - row * ngroups;
   const int G = a.group_eff;
   const WT* w = reinterpret_cast<const WT*>(a.w) + row * a.k + gi * (int64_t)G;
+  if (a.format == WQL_FMT_E4M3) {
+    quantize_e4m3_row(a, w, gid);
+    return;
+  }
+  if (a.format == WQL_FMT_ASYM) {
+    quantize_asym_group(a, w, row, gi, gid);
+    return;
+  }
   const int qmax = a.bits == 4 ? 7 : 127;
   const int qmin = a.bits == 4 ? -8 : -127;
 

@@ -100,6 +100,38 @@ WorkspaceLayout workspace_layout(int64_t m, int64_t n, int32_t topk) {
   return l;
 }
 
+wql_status check_logits_args(const void* x, int32_t x_dtype, int64_t m, const wql_weight* w,
+                             const void* bias, const void* logits_out, int32_t topk,
+                             const void* topk_idx, const void* topk_val, int64_t* g_out) {
+  if (!w || m < 0 || w->n < 0 || w->k <= 0 || w->group < 0) return WQL_EINVAL;
+  if (w->format != WQL_FMT_SYM && w->format != WQL_FMT_E4M3 && w->format != WQL_FMT_ASYM)
+    return WQL_EINVAL;
+  if (topk < 0 || topk > WQL_MAX_TOPK) return WQL_EINVAL;
+  const int64_t n = w->n, k = w->k;
+  if (m > 0 && n > 0) {
+    if (!x || !w->qweight || !w->scales) return WQL_EINVAL;
+    // logits_out may be NULL only for candidates alone (top-K on)
+    if (!logits_out && topk == 0) return WQL_EINVAL;
+    if (topk > 0 && (!topk_idx || !topk_val)) return WQL_EINVAL;
+    if (topk > n) return WQL_EINVAL;
+    if (w->format == WQL_FMT_ASYM && !w->zeros) return WQL_EINVAL;
+  }
+  if (w->bits != 4 && w->bits != 8) return WQL_EUNSUPPORTED;
+  if (w->format == WQL_FMT_E4M3 && (w->bits != 8 || w->group != 0)) return WQL_EUNSUPPORTED;
+  if (w->format == WQL_FMT_ASYM && (w->bits != 4 || w->group == 0 || w->group % 128 != 0))
+    return WQL_EUNSUPPORTED;
+  if (!half_dtype(x_dtype) || !half_dtype(w->scale_dtype)) return WQL_EUNSUPPORTED;
+  const int64_t g = w->group == 0 ? k : w->group;
+  if (k % 64 != 0 || g % 64 != 0 || k % g != 0) return WQL_EUNSUPPORTED;
+  if (n >= (int64_t(1) << 31) || m >= (int64_t(1) << 31) || k >= (int64_t(1) << 30))
+    return WQL_EUNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(w->qweight, 16) || !aligned(w->scales, 2) ||
+      !aligned(logits_out, 2) || !aligned(bias, 2))
+    return WQL_EUNSUPPORTED;
+  *g_out = g;
+  return WQL_OK;
+}
+
 }  // namespace wql
 
 using namespace wql;
@@ -129,9 +161,25 @@ size_t wql_workspace_size(int64_t m, int64_t n, int32_t topk) {
 wql_status wql_quantize(const void* w, int32_t w_dtype, int64_t n, int64_t k, int32_t bits,
                         int32_t group, int32_t scale_dtype, int32_t clip, void* qweight_out,
                         void* scales_out, cudaStream_t stream) {
+  return wql_quantize_ex(w, w_dtype, n, k, WQL_FMT_SYM, bits, group, scale_dtype, clip,
+                         qweight_out, scales_out, nullptr, stream);
+}
+
+wql_status wql_quantize_ex(const void* w, int32_t w_dtype, int64_t n, int64_t k, int32_t format,
+                           int32_t bits, int32_t group, int32_t scale_dtype, int32_t clip,
+                           void* qweight_out, void* scales_out, void* zeros_out,
+                           cudaStream_t stream) {
   if (n < 0 || k <= 0 || group < 0) return WQL_EINVAL;
   if (n > 0 && (!w || !qweight_out || !scales_out)) return WQL_EINVAL;
   if (clip != WQL_CLIP_RTN && clip != WQL_CLIP_MSE) return WQL_EINVAL;
+  if (format != WQL_FMT_SYM && format != WQL_FMT_E4M3 && format != WQL_FMT_ASYM)
+    return WQL_EINVAL;
+  if (format == WQL_FMT_ASYM && n > 0 && !zeros_out) return WQL_EINVAL;
+  if (format == WQL_FMT_E4M3 && (bits != 8 || group != 0 || clip != WQL_CLIP_RTN))
+    return WQL_EUNSUPPORTED;
+  if (format == WQL_FMT_ASYM && (bits != 4 || group == 0 || group % 128 != 0 ||
+                                 clip != WQL_CLIP_RTN))
+    return WQL_EUNSUPPORTED;
   if (bits != 4 && bits != 8) return WQL_EUNSUPPORTED;
   if (w_dtype != WQL_F32 && !half_dtype(w_dtype)) return WQL_EUNSUPPORTED;
   if (!half_dtype(scale_dtype)) return WQL_EUNSUPPORTED;
@@ -151,10 +199,15 @@ wql_status wql_quantize(const void* w, int32_t w_dtype, int64_t n, int64_t k, in
   a.scale_dtype = scale_dtype;
   a.nratios = clip == WQL_CLIP_MSE ? 5 : 1;
   static const double kRatios[5] = {1.0, 0.95, 0.9, 0.85, 0.8};
-  const double qmax = bits == 4 ? 7.0 : 127.0;
+  // the largest code magnitude the scale maps amax (or, asymmetric, the
+  // group's range) to
+  const double qmax = format == WQL_FMT_E4M3 ? 448.0 : format == WQL_FMT_ASYM ? 15.0
+                      : bits == 4 ? 7.0 : 127.0;
   for (int i = 0; i < 5; ++i) a.ratio_c[i] = (float)(kRatios[i] / qmax);
   a.qweight = qweight_out;
   a.scales = static_cast<uint16_t*>(scales_out);
+  a.format = format;
+  a.zeros = static_cast<uint8_t*>(zeros_out);
   cudaError_t e = launch_quantize(a, stream);
   return e == cudaSuccess ? WQL_OK : cuda_fail(e);
 }
@@ -185,24 +238,11 @@ wql_status wql_unpack(const int32_t* packed, int64_t n, int64_t k, uint8_t* nibb
 wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weight* w,
                       const void* bias, void* logits_out, int32_t topk, int32_t* topk_idx,
                       float* topk_val, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  if (!w || m < 0 || w->n < 0 || w->k <= 0 || w->group < 0 || w->reserved != 0)
-    return WQL_EINVAL;
-  if (topk < 0 || topk > WQL_MAX_TOPK) return WQL_EINVAL;
+  int64_t g = 0;
+  const wql_status st = check_logits_args(x, x_dtype, m, w, bias, logits_out, topk, topk_idx,
+                                          topk_val, &g);
+  if (st != WQL_OK) return st;
   const int64_t n = w->n, k = w->k;
-  if (m > 0 && n > 0) {
-    if (!x || !w->qweight || !w->scales || !logits_out) return WQL_EINVAL;
-    if (topk > 0 && (!topk_idx || !topk_val)) return WQL_EINVAL;
-    if (topk > n) return WQL_EINVAL;
-  }
-  if (w->bits != 4 && w->bits != 8) return WQL_EUNSUPPORTED;
-  if (!half_dtype(x_dtype) || !half_dtype(w->scale_dtype)) return WQL_EUNSUPPORTED;
-  const int64_t g = w->group == 0 ? k : w->group;
-  if (k % 64 != 0 || g % 64 != 0 || k % g != 0) return WQL_EUNSUPPORTED;
-  if (n >= (int64_t(1) << 31) || m >= (int64_t(1) << 31) || k >= (int64_t(1) << 30))
-    return WQL_EUNSUPPORTED;
-  if (!aligned(x, 16) || !aligned(w->qweight, 16) || !aligned(w->scales, 2) ||
-      !aligned(logits_out, 2) || !aligned(bias, 2))
-    return WQL_EUNSUPPORTED;
   if (m == 0 || n == 0) return WQL_OK;
   const WorkspaceLayout lay = workspace_layout(m, n, topk);
   // top-K needs a workspace; any workspace given (top-K or not) holds the
@@ -212,7 +252,7 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   const int esz = 2;
   // tokens per decode launch: 16, fewer when x for 16 rows does not fit in
   // shared memory next to the rest
-  const int dchunk = decode_max_tokens((int)k, w->bits, (int)g, topk);
+  const int dchunk = decode_max_tokens((int)k, w->bits, (int)g, topk, w->format);
   if (dchunk < 1) return WQL_EUNSUPPORTED;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -230,6 +270,8 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   base.k = (int)k;
   base.bias = bias;
   base.topk = topk;
+  base.format = w->format;
+  base.zeros = static_cast<const uint8_t*>(w->zeros);
   // the counter block also schedules the decode kernel's work units
   if (ws) base.counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
   if (topk > 0) {
@@ -241,14 +283,18 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   // kernel runs on 16-token slices.
   LogitsArgs probe = base;
   probe.m = (int)(m < 256 ? m : 256);
-  const bool use_tc = m > kDecodeMaxTokens && tc_supported(probe);
+  // (fp8 and zero-point weights, and candidates alone, take the decode
+  // kernel's 16-token slices at every m)
+  const bool use_tc = m > kDecodeMaxTokens && w->format == WQL_FMT_SYM && logits_out &&
+                      tc_supported(probe);
   const int64_t chunk = use_tc ? 256 : dchunk;
   for (int64_t m0 = 0; m0 < m; m0 += chunk) {
     const int64_t mc = (m - m0) < chunk ? (m - m0) : chunk;
     LogitsArgs a = base;
     a.x = static_cast<const unsigned char*>(x) + (size_t)m0 * k * esz;
     a.m = (int)mc;
-    a.logits = static_cast<unsigned char*>(logits_out) + (size_t)m0 * n * esz;
+    a.logits = logits_out ? static_cast<unsigned char*>(logits_out) + (size_t)m0 * n * esz
+                          : nullptr;
     if (topk > 0) {
       a.topk_idx = topk_idx + (size_t)m0 * topk;
       a.topk_val = topk_val + (size_t)m0 * topk;
@@ -269,8 +315,10 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
 
 wql_status wql_embed_gather(const int32_t* ids, int64_t t, const wql_weight* w,
                             int32_t out_dtype, void* out, cudaStream_t stream) {
-  if (!w || t < 0 || w->n < 0 || w->k <= 0 || w->group < 0 || w->reserved != 0)
+  if (!w || t < 0 || w->n < 0 || w->k <= 0 || w->group < 0) return WQL_EINVAL;
+  if (w->format != WQL_FMT_SYM && w->format != WQL_FMT_E4M3 && w->format != WQL_FMT_ASYM)
     return WQL_EINVAL;
+  if (w->format != WQL_FMT_SYM) return WQL_EUNSUPPORTED;
   const int64_t n = w->n, k = w->k;
   if (t > 0 && (!ids || !out)) return WQL_EINVAL;
   if (t > 0 && n > 0 && (!w->qweight || !w->scales)) return WQL_EINVAL;

@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -222,6 +223,35 @@ template <> struct OffsetCodes<8, __nv_bfloat16> {   // exact q (no offset)
   }
 };
 
+// fp8 e4m3 codes (four per word, element j in byte j) -> two packed pairs in
+// natural order, exact: every e4m3 value is an fp16 normal or zero (the
+// subnormals m * 2^-9 included) and fits bf16's 8-bit mantissa too.
+template <typename XT> struct E4M3Codes;
+template <> struct E4M3Codes<__half> {
+  static constexpr float kOffset = 0.0f;
+  static constexpr int kPairs = 2;
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t (&out)[2]) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+    out[0] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+    out[1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+  }
+};
+template <> struct E4M3Codes<__nv_bfloat16> {
+  static constexpr float kOffset = 0.0f;
+  static constexpr int kPairs = 2;
+  static __device__ __forceinline__ void run(uint32_t w, uint32_t (&out)[2]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2_raw r =
+          __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w >> (16 * h)) & 0xFFFFu), __NV_E4M3);
+      const __nv_bfloat162 b = __floats2bfloat162_rn(__half2float(__ushort_as_half(r.x)),
+                                                     __half2float(__ushort_as_half(r.y)));
+      out[h] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+  }
+};
+
 // fp16 int4 with activations pre-scaled by 1/16 at the elements held in
 // nibbles 1 and 3 of each half-word (elements 2, 3, 6, 7 of a word): those
 // nibbles stay where they are and read as 1024 + 16u, so only one shift per
@@ -405,6 +435,8 @@ struct QuantizeArgs {
   float ratio_c[5];          // fl32(r / qmax), computed on the host in binary64
   void* qweight;
   uint16_t* scales;
+  int format;                // wql_format
+  uint8_t* zeros;            // WQL_FMT_ASYM: [n, k / group_eff]
 };
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 cudaError_t launch_pack(const uint8_t* nib, int64_t n, int64_t k, uint32_t* out, cudaStream_t s);
@@ -430,13 +462,22 @@ struct LogitsArgs {
                               // (zero between calls)
   int weights_static;         // 1: no kernel that may precede this launch on the
                               // stream writes qweight / scales
+  int format;                 // wql_format of the weight
+  const uint8_t* zeros;       // WQL_FMT_ASYM: [n, k / group_eff] zero points
 };
+// Host checks shared by the logits entry points (no CUDA call): argument
+// validity, the weight's format, sizes and alignment.  On WQL_OK, *g_out is
+// the effective group (k for one scale per row).
+wql_status check_logits_args(const void* x, int32_t x_dtype, int64_t m, const wql_weight* w,
+                             const void* bias, const void* logits_out, int32_t topk,
+                             const void* topk_idx, const void* topk_val, int64_t* g_out);
+
 // Bandwidth-bound path for m <= 16 (warp MMA fed straight from global memory,
 // split over vocab rows).  `err` is the workspace's sticky error word.
 cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s);
-size_t decode_smem_bytes(int m, int k, int bits, int group_eff, int topk);
+size_t decode_smem_bytes(int m, int k, int bits, int group_eff, int topk, int format);
 // Most token rows one decode launch takes for this shape (0: none fits).
-int decode_max_tokens(int k, int bits, int group_eff, int topk);
+int decode_max_tokens(int k, int bits, int group_eff, int topk, int format);
 // Tensor-core path for 16 < m <= 256 (fp16 activations and scales): logits
 // only (a.topk is ignored; launch_topk_select follows it).
 bool tc_supported(const LogitsArgs& a);
