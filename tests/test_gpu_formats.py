@@ -19,7 +19,7 @@ import oracle
 import weight_only_quantized_wql_gb300 as wql
 from weight_only_quantized_wql_gb300 import synth
 from parity import (NTHREADS, assert_logits_close, check_topk, np_bits, np_input,
-                    oracle_quantized, to_f64)
+                    oracle_quantized, report_ties, to_f64)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -100,7 +100,7 @@ def test_fp8_logits(xdt, sdt, m):
     assert_logits_close(to_f64(logits), ref, absacc, f"fp8 m={m}")
     g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
     ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K) for r in range(m))
-    assert ties == 0, f"{ties} near-tie swaps"
+    report_ties(f"fp8 m={m}", ties, m)
 
 
 def test_fp8_fullsize_head_m1():
@@ -167,7 +167,7 @@ def test_asym_logits(xdt, sdt, m, k, group):
     assert_logits_close(to_f64(logits), ref, absacc, f"asym m={m}")
     g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
     ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K) for r in range(m))
-    assert ties == 0, f"{ties} near-tie swaps"
+    report_ties(f"asym m={m} g{group}", ties, m)
 
 
 # ---------------------------------------------------------------------------
@@ -196,4 +196,4 @@ def test_candidates_only(bits, group, m):
                                 oracle.F16, group, n, k, nthreads=NTHREADS)
     g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
     ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K) for r in range(m))
-    assert ties == 0, f"{ties} near-tie swaps"
+    report_ties(f"candidates_only w{bits}g{group} m={m}", ties, m)
