@@ -164,8 +164,9 @@ wql_status wql_unpack(const int32_t* packed, int64_t n, int64_t k,
 /* Bytes of workspace wql_logits needs for m token rows and top-K width topk
  * (n is the vocab size; the need does not grow with it).  Pure host
  * arithmetic; never touches the GPU.  The buffer must be zero-filled once
- * before its first use; every call leaves it ready for the next.  Calls that
- * may run concurrently need separate workspaces. */
+ * before its first use; every call leaves it ready for the next (except for
+ * the sticky error word of a timed-out wait, see wql_debug_set_waits).
+ * Calls that may run concurrently need separate workspaces. */
 size_t wql_workspace_size(int64_t m, int64_t n, int32_t topk);
 
 /* Logits of a quantised lm_head ("Fused WNA16 GEMM for tied quantized lm_head
@@ -270,6 +271,22 @@ wql_status wql_embed_gather(const int32_t* ids, int64_t t, const wql_weight* w,
 
 /* Static text for a status code. */
 const char* wql_status_string(wql_status status);
+
+/* Diagnostics, for tests of the timeout path.  Every wait inside the kernels
+ * is bounded; a wait that runs out records bit 2 (tensor-core kernel) or 4
+ * (top-K selection) in the workspace's error word (bytes 4..7, sticky until
+ * the caller zeroes it), the kernel finishes without leaving copies or
+ * tensor-core work in flight, and from then on the top-K outputs of every
+ * call on that workspace read index -1 and value NaN.
+ *   budget_cycles  SM cycles a wait of the tensor-core kernel on a ring slot
+ *                  or on data may take (0: the default, about 1 s); the
+ *                  waits for a CTA's own copies keep the default
+ *   stall_mma      1: the tensor-core kernel's MMA warp first waits on a
+ *                  barrier nothing arrives on, so that its budget runs out
+ *                  and every other role's waits run out after it
+ * Process-wide, for the calls launched after it; not for concurrent use.
+ * (The decode kernel, m <= 16, has no waits.) */
+wql_status wql_debug_set_waits(int64_t budget_cycles, int32_t stall_mma);
 
 /* Text of the last CUDA error seen by this host thread ("" if none). */
 const char* wql_last_error(void);

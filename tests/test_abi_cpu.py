@@ -187,3 +187,9 @@ def test_missing_library_raises(monkeypatch):
     monkeypatch.setattr(_build, "LIB", "/nonexistent/libwql.so")
     with pytest.raises(RuntimeError, match="libwql.so not found"):
         wql.load(build_if_missing=False)
+
+
+def test_debug_set_waits_rejects_bad_arguments(lib):
+    assert lib.wql_debug_set_waits(-1, 0) == EINVAL
+    assert lib.wql_debug_set_waits(0, 2) == EINVAL
+    assert lib.wql_debug_set_waits(0, 0) == OK

@@ -30,7 +30,7 @@ from . import _build
 __all__ = [
     "WQLError", "QuantizedWeight", "Workspace", "load", "wql_quantize", "wql_pack",
     "wql_unpack", "wql_workspace_size", "wql_logits", "wql_logits_noalloc", "wql_topk_rescore",
-    "wql_embed_gather",
+    "wql_embed_gather", "wql_debug_set_waits",
     "wql_status_string", "wql_last_error", "wql_launch_count", "F32", "F16", "BF16",
     "CLIP_RTN", "CLIP_MSE", "MAX_TOPK", "NOALLOC_SCRATCH_BYTES", "FMT_SYM", "FMT_E4M3",
     "FMT_ASYM",
@@ -114,6 +114,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.wql_last_error.argtypes = []
         lib.wql_launch_count.restype = ctypes.c_uint64
         lib.wql_launch_count.argtypes = []
+        lib.wql_debug_set_waits.restype = i32
+        lib.wql_debug_set_waits.argtypes = [i64, i32]
         _lib = lib
         return lib
 
@@ -199,6 +201,11 @@ class Workspace:
             return 0
         return int(self.buf[4:8].view(torch.int32).item())
 
+    def clear_error(self) -> None:
+        """Zero the sticky error word (ordered on the current stream)."""
+        if self.buf is not None:
+            self.buf[4:8].zero_()
+
 
 _default_ws: dict = {}
 
@@ -213,6 +220,12 @@ def wql_last_error() -> str:
 
 def wql_launch_count() -> int:
     return int(load().wql_launch_count())
+
+
+def wql_debug_set_waits(budget_cycles: int = 0, stall_mma: bool = False) -> None:
+    """Diagnostics for the timeout path (see wql.h); (0, False) restores the
+    defaults."""
+    _check("wql_debug_set_waits", load().wql_debug_set_waits(budget_cycles, int(stall_mma)))
 
 
 _ws_sizes: dict = {}

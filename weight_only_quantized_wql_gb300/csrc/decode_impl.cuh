@@ -987,6 +987,7 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
       warp_topk_of<16>(nsrc * K, K, [&](int i) { return __ldcg(slots + i); }, best);
       mine = pick(best, lane);
     }
+    if (__ldcg(a.counter + 1) != 0u) mine = kEmptyKey;   // a recorded timeout voids results
     if (lane < K) {
       a.topk_idx[(size_t)tk * K + lane] = mine != kEmptyKey ? key_index(mine) : -1;
       a.topk_val[(size_t)tk * K + lane] = mine != kEmptyKey ? key_value(mine) : __int_as_float(0x7FC00000);

@@ -73,6 +73,9 @@ struct TcParams {
   int sbuf_bytes;       // one tile's scale rows (128 x ngroups halves), 0 = no staging
   int scales_aligned;   // scale table 16-byte aligned
   unsigned int* err;
+  long long wait_budget;  // SM cycles a wait on a ring slot or on data may take
+  int diag_stall;         // diagnostics: the MMA warp first waits on a barrier
+                          // nothing arrives on (the timeout path runs)
 };
 
 __host__ __device__ constexpr uint32_t rup(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -190,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* s_full = acc_empty + 2;        // per-tile scale rows (2 slots)
   uint64_t* s_empty = s_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_empty + 2);
+  uint64_t* stall_bar = s_empty + 2;       // never arrived on (diagnostics)
+  uint64_t* drain_bar = stall_bar + 1;     // the MMA warp's last MMAs, on a timeout
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   unsigned int* flags = tmem_slot + 1;   // [0] bad
 
   const LogitsArgs& a = p.a;
@@ -220,6 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[s], 1);
       mbar_init(&s_empty[s], kDequantWarps);
     }
+    mbar_init(stall_bar, 1);
+    mbar_init(drain_bar, 1);
     flags[0] = 0u;
     fence_barrier_init();
   }
@@ -252,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this tile's scale rows, when the tile is whole and the table aligned
         if (p.sbuf_bytes > 0 && p.scales_aligned && (t + 1) * kTileRows <= n) {
           const int slot = sfills & 1;
-          if (sfills >= 2) bad = !mbar_wait(&s_empty[slot], (uint32_t)(((sfills - 2) >> 1) & 1));
+          if (sfills >= 2) bad = !mbar_wait(&s_empty[slot], (uint32_t)(((sfills - 2) >> 1) & 1), p.wait_budget);
           if (bad) break;
           const uint32_t sbytes = (uint32_t)(kTileRows * p.ngroups * 2);
           mbar_arrive_expect_tx(&s_full[slot], sbytes);
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++sfills;
         }
         for (int c = 0; c < p.chunks && !bad; ++c) {
-          if (wfills >= p.wstages) bad = !mbar_wait(&w_empty[ws], wph ^ 1u);
+          if (wfills >= p.wstages) bad = !mbar_wait(&w_empty[ws], wph ^ 1u, p.wait_budget);
           if (bad) break;
           mbar_arrive_expect_tx(&w_full[ws], (uint32_t)kWChunkBytes);
           tma_load_2d(sm + p.off_w + ws * kWChunkBytes, &tw, c * 32, t * kTileRows, &w_full[ws]);
@@ -288,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t xph = 0;
         for (int t = T0; t < T1 && !bad; ++t)
           for (int kb = 0; kb < p.kblocks && !bad; ++kb) {
-            if (xfills >= p.xstages) bad = !mbar_wait(&x_empty[xs], xph ^ 1u);
+            if (xfills >= p.xstages) bad = !mbar_wait(&x_empty[xs], xph ^ 1u, p.wait_budget);
             if (bad) break;
             mbar_arrive_expect_tx(&x_full[xs], xblock_bytes);
             tma_load_2d(sm + p.off_x + xs * xblock_bytes, &tx, kb * 64, 0, &x_full[xs]);
@@ -319,15 +326,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int as = 0, xs = 0, acc = 0;
     uint32_t aph = 0, xph = 0, accph = 0;
     int tiles_done = 0;
-    if (p.x_resident && T0 < T1) bad = !mbar_wait(&x_full[0], 0u);
+    bool issued = false;
+    if (p.diag_stall) bad = !mbar_wait(stall_bar, 0u, p.wait_budget);
+    if (p.x_resident && T0 < T1 && !bad) bad = !mbar_wait(&x_full[0], 0u, p.wait_budget);
     for (int t = T0; t < T1; ++t, ++tiles_done) {
       // wait for the epilogue to have drained this accumulator buffer
-      if (!bad && tiles_done >= p.acc_bufs) bad = !mbar_wait(&acc_empty[acc], accph ^ 1u);
+      if (!bad && tiles_done >= p.acc_bufs) bad = !mbar_wait(&acc_empty[acc], accph ^ 1u, p.wait_budget);
       if (__any_sync(0xFFFFFFFFu, bad)) { bad = true; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.npad);
       for (int kb0 = 0; kb0 < p.kblocks; kb0 += kStageBlocks) {
-        bad = !mbar_wait(&a_full[as], aph);
+        bad = !mbar_wait(&a_full[as], aph, p.wait_budget);
         if (__any_sync(0xFFFFFFFFu, bad)) { bad = true; break; }
         tc_fence_after();
         const int nb = min(kStageBlocks, p.kblocks - kb0);
@@ -335,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int sb = 0; sb < nb; ++sb) {
           const int kb = kb0 + sb;
           if (!p.x_resident) {
-            bad = !mbar_wait(&x_full[xs], xph);
+            bad = !mbar_wait(&x_full[xs], xph, p.wait_budget);
             if (__any_sync(0xFFFFFFFFu, bad)) { bad = true; break; }
             tc_fence_after();
           }
@@ -348,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_f16(d_tmem, ad + 3 * kKStep, xd + 3 * kKStep, idesc, 1u);
             if (!p.x_resident) umma_commit(&x_empty[xs]);   // activation block consumed
           }
+          issued = true;
           __syncwarp();
           if (!p.x_resident && ++xs == p.xstages) { xs = 0; xph ^= 1u; }
         }
@@ -360,6 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) umma_commit(&acc_full[acc]);  // accumulator ready for the epilogue
       __syncwarp();
       if (++acc == p.acc_bufs) { acc = 0; accph ^= 1u; }
+    }
+    if (bad && issued) {
+      // after a timeout: the MMAs already issued finish before TMEM is freed
+      if (leader) umma_commit(drain_bar);
+      __syncwarp();
+      mbar_wait(drain_bar, 0u);
     }
   } else if (warp < kEpilogueWarp0) {
     // ------------------------------ dequantisers ------------------------------
@@ -386,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = sfills & 1;
       const uint16_t* srow;
       if (staged) {
-        if (!bad) bad = !mbar_wait(&s_full[slot], (uint32_t)((sfills >> 1) & 1));
+        if (!bad) bad = !mbar_wait(&s_full[slot], (uint32_t)((sfills >> 1) & 1), p.wait_budget);
         srow = reinterpret_cast<const uint16_t*>(sm + p.off_s + slot * p.sbuf_bytes) +
                r * p.ngroups;
       } else {
@@ -425,18 +441,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c = (st * kStageBlocks) / kBlocksPerChunk;
         if (c != cur_chunk) {
           if (cur_chunk >= 0) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&w_empty[ws]);
+            // a warp that gave up releases nothing more: the producer then
+            // times out too instead of refilling a slot whose copy may fly
+            bad = __any_sync(0xFFFFFFFFu, bad);
+            if (lane == 0 && !bad) mbar_arrive(&w_empty[ws]);
             if (++ws == p.wstages) { ws = 0; wph ^= 1u; }
           }
-          if (!bad) bad = !mbar_wait(&w_full[ws], wph);
+          if (!bad) bad = !mbar_wait(&w_full[ws], wph, p.wait_budget);
           cur_chunk = c;
         }
         const unsigned int js = js0 + (unsigned int)st;
         const int as = (int)(js % (unsigned int)p.astages);
         // the buffer's previous fill (astages stages back) must be consumed
         if (js >= (unsigned int)p.astages && !bad)
-          bad = !mbar_wait(&a_empty[as], ((js / (unsigned int)p.astages) & 1u) ^ 1u);
+          bad = !mbar_wait(&a_empty[as], ((js / (unsigned int)p.astages) & 1u) ^ 1u, p.wait_budget);
         if (have && !bad) {
           const int b = kb % kBlocksPerChunk;
           const uint32_t wrow = base + p.off_w + ws * kWChunkBytes + r * 128;
@@ -481,17 +499,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_async_smem();                   // generic-proxy writes -> tensor core
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[as]);
+        bad = __any_sync(0xFFFFFFFFu, bad);
+        if (lane == 0 && !bad) mbar_arrive(&a_full[as]);
       }
       if (cur_chunk >= 0) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&w_empty[ws]);
+        bad = __any_sync(0xFFFFFFFFu, bad);
+        if (lane == 0 && !bad) mbar_arrive(&w_empty[ws]);
         if (++ws == p.wstages) { ws = 0; wph ^= 1u; }
       }
       if (staged) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[slot]);
+        bad = __any_sync(0xFFFFFFFFu, bad);
+        if (lane == 0 && !bad) mbar_arrive(&s_empty[slot]);
         ++sfills;
       }
     }
@@ -504,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t accph = 0;
     for (int t = T0; t < T1; ++t) {
-      if (!bad) bad = !mbar_wait(&acc_full[acc], accph);
+      if (!bad) bad = !mbar_wait(&acc_full[acc], accph, p.wait_budget);
       bad = __any_sync(0xFFFFFFFFu, bad);
       tc_fence_after();
       const int row = t * kTileRows + r;
@@ -554,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (lane == 0 && !bad) mbar_arrive(&acc_empty[acc]);
       if (++acc == p.acc_bufs) { acc = 0; accph ^= 1u; }
     }
   }
@@ -664,6 +682,8 @@ cudaError_t launch_tc(const LogitsArgs& a, unsigned int* err, cudaStream_t s) {
   TcParams p{};
   p.a = a;
   p.err = err;
+  p.wait_budget = diag_wait_budget();
+  p.diag_stall = diag_stall_mma();
   p.tiles_total = (a.n + kTileRows - 1) / kTileRows;
   p.npad = (a.m + 15) / 16 * 16;
   p.kblocks = a.k / 64;

@@ -528,7 +528,10 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const LogitsAr
     for (int i = lane; i < parts * K; i += 32) list_insert<KT>(list, __ldcg(slots + i));
     unsigned long long outk[KT];
     warp_merge_topk_redux<KT>(list, K, outk);
-    const unsigned long long b = pick(outk, lane);
+    // a timed-out wait of this call's kernels (or an earlier one's, until
+    // the caller clears the error word) voids the result
+    const bool failed = __ldcg(a.counter + 1) != 0u;
+    const unsigned long long b = failed ? kEmptyKey : pick(outk, lane);
     if (lane < K) {
       a.topk_idx[(size_t)tok * K + lane] = b == kEmptyKey ? -1 : key_index(b);
       a.topk_val[(size_t)tok * K + lane] =

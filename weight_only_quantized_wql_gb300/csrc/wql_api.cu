@@ -100,6 +100,17 @@ WorkspaceLayout workspace_layout(int64_t m, int64_t n, int32_t topk) {
   return l;
 }
 
+namespace {
+std::atomic<long long> g_wait_budget{0};
+std::atomic<int> g_stall_mma{0};
+}  // namespace
+
+long long diag_wait_budget() {
+  const long long b = g_wait_budget.load(std::memory_order_relaxed);
+  return b > 0 ? b : kWaitBudgetCycles;
+}
+int diag_stall_mma() { return g_stall_mma.load(std::memory_order_relaxed); }
+
 wql_status check_logits_args(const void* x, int32_t x_dtype, int64_t m, const wql_weight* w,
                              const void* bias, const void* logits_out, int32_t topk,
                              const void* topk_idx, const void* topk_val, int64_t* g_out) {
@@ -375,6 +386,13 @@ wql_status wql_topk_rescore(const void* x, int32_t x_dtype, int64_t m, const voi
   a.logits = logits_inout;
   cudaError_t e = launch_rescore(a, stream);
   return e == cudaSuccess ? WQL_OK : cuda_fail(e);
+}
+
+wql_status wql_debug_set_waits(int64_t budget_cycles, int32_t stall_mma) {
+  if (budget_cycles < 0 || (stall_mma != 0 && stall_mma != 1)) return WQL_EINVAL;
+  g_wait_budget.store(budget_cycles, std::memory_order_relaxed);
+  g_stall_mma.store(stall_mma, std::memory_order_relaxed);
+  return WQL_OK;
 }
 
 }  // extern "C"

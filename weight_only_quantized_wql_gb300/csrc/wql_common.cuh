@@ -465,6 +465,12 @@ struct LogitsArgs {
   int format;                 // wql_format of the weight
   const uint8_t* zeros;       // WQL_FMT_ASYM: [n, k / group_eff] zero points
 };
+// Diagnostics (wql_debug_set_waits): the budget of the tensor-core kernel's
+// in-loop waits, in SM cycles, and whether its MMA warp first stalls on a
+// barrier nothing arrives on.
+long long diag_wait_budget();
+int diag_stall_mma();
+
 // Host checks shared by the logits entry points (no CUDA call): argument
 // validity, the weight's format, sizes and alignment.  On WQL_OK, *g_out is
 // the effective group (k for one scale per row).
