@@ -135,7 +135,6 @@ cudaError_t launch_decode(const LogitsArgs& a, unsigned int* err, cudaStream_t s
   p.off_cnt = P.off_cnt;
   p.off_misc = P.off_misc;
   p.cap = P.cap;
-  p.asym = a.format == WQL_FMT_ASYM ? 1 : 0;
   p.xsum_off = P.xsum_off;
   p.corr_floats = P.corr_floats;
   // linear scale addressing: with two group halves per step, groups of 64

@@ -95,7 +95,6 @@ struct DecodeParams {
   uint32_t xpitch;   // bytes per token row of x in shared memory
   uint32_t off_x, off_zero, off_corr, off_ring, off_list, off_cnt, off_misc, off_ugrp;
   int early_weights;  // 1: weights may be read before the preceding kernel ends
-  int asym;           // int4 codes with a zero point per group (no half steps)
   int xsum_off;       // floats from the offset sums to the plain sums of x (asym)
   int corr_floats;    // floats of both (cleared at launch)
 };
@@ -372,9 +371,10 @@ __device__ __forceinline__ void compact(const Cands& C, int tk, int K) {
 // halves, groups of 64 columns with the two halves' entries adjacent and
 // 4-byte aligned (one 32-bit load); otherwise one group per step.  Without
 // LIN they are looked up per step in a unit -> group table.
-template <int BITS, bool GW2, bool LIN, typename XT, typename ST, int NT, bool F8>
+template <int BITS, bool GW2, bool LIN, typename XT, typename ST, int NT, int FMT>
 __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr bool F8 = FMT == WQL_FMT_E4M3;
   using Codes = typename CodesOf<BITS, XT, F8>::type;
   constexpr int W = warps_of(NT);
   constexpr int kThr = W * 32;
@@ -384,7 +384,8 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
   constexpr uint32_t kXStepBytes = kStepCols * 2;       // x bytes per step
   constexpr bool kHasOffset = !F8 && !(BITS == 8 && std::is_same<XT, __nv_bfloat16>::value);
   // zero points: int4 with one group per step only (the host enforces it)
-  constexpr bool kMayAsym = BITS == 4 && !GW2;
+  constexpr bool kAsym = FMT == WQL_FMT_ASYM;
+  static_assert(!kAsym || (BITS == 4 && !GW2), "zero points: int4, one group per step");
 
   extern __shared__ __align__(128) uint8_t sm[];
   const LogitsArgs& a = p.a;
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
         const int gi = LIN ? j : ugrp[BITS == 4 ? 2 * s : s];
         SA = ldg_scale(rp.spa + gi);
         SB = ldg_scale(rp.spb + gi);
-        if (kMayAsym && p.asym) {   // the zero points ride in the upper halves
+        if constexpr (kAsym) {      // the zero points ride in the upper halves
           SA |= ldg_u8(a.zeros + (rp.spa - scales) + gi) << 16;
           SB |= ldg_u8(a.zeros + (rp.spb - scales) + gi) << 16;
         }
@@ -558,7 +559,7 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
       }
       float xplain[kB];   // plain sums of the pieces (zero points)
 #pragma unroll
-      for (int b = 0; b < kB; ++b) xplain[b] = kMayAsym && p.asym ? piece_sum<XT>(v[b]) : 0.f;
+      for (int b = 0; b < kB; ++b) xplain[b] = kAsym ? piece_sum<XT>(v[b]) : 0.f;
 #pragma unroll
       for (int b = 0; b < kB; ++b) {
         if (i0 + b * kThr >= total) continue;
@@ -569,7 +570,7 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
         const uint32_t q = (uint32_t)pc[b];
         const uint32_t phys = (q & ~7u) | ((q ^ x_swz<GW2>(tk[b])) & 7u);
         *reinterpret_cast<uint4*>(xs + (size_t)tk[b] * p.xpitch + phys * 16) = v[b];
-        if (kMayAsym && p.asym && pc[b] < kp)
+        if (kAsym && pc[b] < kp)
           atomicAdd(&corr[p.xsum_off + (pc[b] / (kStepCols / 8)) * kMaxTok + tk[b]], xplain[b]);
         if (kHasOffset && pc[b] < kp) {
           const float o = offset_sum<BITS, XT>(v[b]);
@@ -776,7 +777,7 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
     } else {
       const float fa = scale_bits_to_f32<ST>((uint16_t)scA);
       const float fb = scale_bits_to_f32<ST>((uint16_t)scB);
-      if (kMayAsym && p.asym) {
+      if constexpr (kAsym) {
         // zero points: sum x*(u - z) = sum x*(u - 8) + (8 - z) * sum x
         const float da = 8.0f - (float)(scA >> 16), db = 8.0f - (float)(scB >> 16);
 #pragma unroll
@@ -997,9 +998,9 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
   if (threadIdx.x == 0) *a.counter = 0u;
 }
 
-template <int BITS, bool GW2, bool LIN, typename XT, typename ST, int NT, bool F8 = false>
+template <int BITS, bool GW2, bool LIN, typename XT, typename ST, int NT, int FMT = WQL_FMT_SYM>
 cudaError_t launch_t(const DecodeParams& p, size_t smem, int ctas, cudaStream_t s) {
-  auto kern = decode_kernel<BITS, GW2, LIN, XT, ST, NT, F8>;
+  auto kern = decode_kernel<BITS, GW2, LIN, XT, ST, NT, FMT>;
   // per instantiation: raise the dynamic smem limit when a launch needs more,
   // and ask for the smallest shared-memory carveout that holds it, leaving
   // the rest of the SM's 256 KB to L1 (scale rows are read through L1)
@@ -1041,13 +1042,17 @@ cudaError_t dispatch_lin(const DecodeParams& p, bool gw2, int nt, size_t smem, i
     if (nt == 2) return launch_t<4, true, LIN, XT, ST, 2>(p, smem, ctas, s);
     return launch_t<4, true, LIN, XT, ST, 4>(p, smem, ctas, s);
   }
+  if (p.a.bits == 4 && p.a.format == WQL_FMT_ASYM) {
+    if (nt == 1) return launch_t<4, false, LIN, XT, ST, 1, WQL_FMT_ASYM>(p, smem, ctas, s);
+    return launch_t<4, false, LIN, XT, ST, 2, WQL_FMT_ASYM>(p, smem, ctas, s);
+  }
   if (p.a.bits == 4) {
     if (nt == 1) return launch_t<4, false, LIN, XT, ST, 1>(p, smem, ctas, s);
     return launch_t<4, false, LIN, XT, ST, 2>(p, smem, ctas, s);
   }
   if (p.a.format == WQL_FMT_E4M3) {
-    if (nt == 1) return launch_t<8, false, LIN, XT, ST, 1, true>(p, smem, ctas, s);
-    return launch_t<8, false, LIN, XT, ST, 2, true>(p, smem, ctas, s);
+    if (nt == 1) return launch_t<8, false, LIN, XT, ST, 1, WQL_FMT_E4M3>(p, smem, ctas, s);
+    return launch_t<8, false, LIN, XT, ST, 2, WQL_FMT_E4M3>(p, smem, ctas, s);
   }
   if (nt == 1) return launch_t<8, false, LIN, XT, ST, 1>(p, smem, ctas, s);
   return launch_t<8, false, LIN, XT, ST, 2>(p, smem, ctas, s);
