@@ -77,6 +77,15 @@ typedef enum wql_format {
                         lm_head model of its lm-eval table) */
 } wql_format;
 
+/* wql_weight.format = a wql_format, optionally ORed with flags: */
+#define WQL_FMT_MASK 0xFF
+/* WQL_WEIGHT_STATIC: no kernel that may run before a call on its stream writes
+ * this weight (qweight, scales, zeros) -- it was written once, before.  The
+ * decode kernel then starts copying it before the preceding kernel on the
+ * stream has finished (programmatic dependent launch); X, the workspace and
+ * the outputs are still touched only after it. */
+#define WQL_WEIGHT_STATIC 0x100
+
 /* A quantised lm_head weight as produced by wql_quantize() / wql_quantize_ex().
  *   bits 4: qweight is int32 [n, k/8]; word i of a row holds elements
  *           8i .. 8i+7, element 8i + j in the nibble at position
@@ -98,7 +107,8 @@ typedef struct wql_weight {
   int32_t bits;         /* 4 or 8 */
   int32_t group;        /* G (multiple of 64) or 0 = one scale per row */
   int32_t scale_dtype;  /* WQL_F16 or WQL_BF16 */
-  int32_t format;       /* wql_format; WQL_FMT_SYM (0) for the layouts above */
+  int32_t format;       /* wql_format (WQL_FMT_SYM = 0 for the layouts above),
+                           optionally | WQL_WEIGHT_STATIC */
   int64_t n;            /* vocab rows */
   int64_t k;            /* hidden size */
   const void* qweight;  /* device */

@@ -69,6 +69,8 @@ def test_logits_argument_checks(lib):
     assert _logits(lib, None) == EINVAL
     assert _logits(lib, _weight(), m=-1) == EINVAL
     assert _logits(lib, _weight(fmt=7)) == EINVAL                # unknown format
+    assert _logits(lib, _weight(fmt=0x200)) == EINVAL            # unknown flag
+    assert _logits(lib, _weight(fmt=0x100), m=0) == OK           # static-weights flag
     assert _logits(lib, _weight(), x=None) == EINVAL
     assert _logits(lib, _weight(), out=None) == EINVAL           # no logits and no top-K
     assert _logits(lib, _weight(q=None)) == EINVAL

@@ -39,6 +39,7 @@ __all__ = [
 F32, F16, BF16 = 0, 1, 2
 CLIP_RTN, CLIP_MSE = 0, 1
 FMT_SYM, FMT_E4M3, FMT_ASYM = 0, 1, 2    # wql_format
+WEIGHT_STATIC = 0x100                    # flag ORed into the format field
 MAX_TOPK = 16
 MAX_CTAS = 1024
 _DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
@@ -159,6 +160,8 @@ class QuantizedWeight:
     k: int
     fmt: int = FMT_SYM         # wql_format
     zeros: torch.Tensor | None = None   # uint8 [n, k/group] zero points (FMT_ASYM)
+    static: bool = False       # WQL_WEIGHT_STATIC: never written after quantisation, so
+                               # calls may read it before the preceding kernel ends
 
     @property
     def scale_dtype(self) -> int:
@@ -168,10 +171,11 @@ class QuantizedWeight:
         # built once per (qweight, scales) storage; calls reuse it
         zp = self.zeros.data_ptr() if self.zeros is not None else None
         key = (self.qweight.data_ptr(), self.scales.data_ptr(), self.bits, self.group,
-               self.n, self.k, self.scales.dtype, self.fmt, zp)
+               self.n, self.k, self.scales.dtype, self.fmt, zp, self.static)
         cached = self.__dict__.get("_st")
         if cached is None or cached[0] != key:
-            cached = (key, _WqlWeight(self.bits, self.group, self.scale_dtype, self.fmt,
+            fmt = self.fmt | (WEIGHT_STATIC if self.static else 0)
+            cached = (key, _WqlWeight(self.bits, self.group, self.scale_dtype, fmt,
                                       self.n, self.k, key[0], key[1], zp))
             self.__dict__["_st"] = cached
         return cached[1]

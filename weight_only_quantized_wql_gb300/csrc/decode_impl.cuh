@@ -45,10 +45,8 @@
 //    compared against the threshold; the few that reach it are appended.  A
 //    buffer about to overflow is compacted to its K best, which raises the
 //    threshold.  At the end the CTA takes, per token, the K best of its
-//    warps' buffers (K rounds of a warp maximum: over each warp's sorted K
-//    best, merged from registers, with one or two tokens; over all buffers
-//    at once with more) and writes them, sorted, to its slot of the
-//    workspace.  The last CTA to take the ticket (acquire-release atomic)
+//    warps' buffers (K rounds of a warp maximum over all buffers at once)
+//    and writes them, sorted, to its slot of the workspace.  The last CTA to take the ticket (acquire-release atomic)
 //    reads every slot's first entry; only the slots holding the K largest
 //    first entries can hold any of the final K, so it merges those K sorted
 //    slots.
@@ -521,17 +519,17 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
   // otherwise after it.
   const int tile_b = T0 + (rb < re ? rb / rpt : 0);
   const int r_b = rb < re ? rb % rpt : 0;
+  const RunPtr run0 = run_ptr(tile_b, r_b, rb < re);
+  uint32_t sa[kPD], sb[kPD];
   if (p.early_weights) {
-    const RunPtr r0 = run_ptr(tile_b, r_b, rb < re);
 #pragma unroll
-    for (int j = 0; j < kPD; ++j) copy_step(r0, j);
+    for (int j = 0; j < kPD; ++j) copy_step(run0, j);
   }
   griddep_launch_dependents();
   griddep_wait();
   if (!p.early_weights) {
-    const RunPtr r0 = run_ptr(tile_b, r_b, rb < re);
 #pragma unroll
-    for (int j = 0; j < kPD; ++j) copy_step(r0, j);
+    for (int j = 0; j < kPD; ++j) copy_step(run0, j);
   }
   __syncthreads();   // the cleared offset sums before the atomics below
 
@@ -801,8 +799,7 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
 
   // ---- main loop over this warp's runs ----
   int cur_tile = tile_b, cur_r = r_b;
-  RunPtr cur = run_ptr(cur_tile, cur_r, rb < re);
-  uint32_t sa[kPD], sb[kPD];
+  RunPtr cur = run0;
 #pragma unroll
   for (int j = 0; j < kPD; ++j) load_scales(cur, j, sa[j], sb[j]);
   for (int q = rb; q < re; ++q) {
@@ -901,32 +898,19 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
 
   // ---- top-K of this CTA ----
   // Every warp's buffer holds, per token, all of its values that can be
-  // among its K best.  With up to four tokens each warp sorts its own
-  // buffers' K best (a compaction), then warp tk merges the W sorted lists
-  // of token tk; with more tokens warp tk takes the K best of the W buffers
-  // at once (lane l holding entry l of every buffer).  The CTA's K best go,
-  // best first, to its slot in the workspace.
+  // among its K best.  Warp tk takes the K best of the W buffers of token tk
+  // at once (lane l holds entry l of every buffer: K rounds of a warp
+  // maximum) and writes them, best first, to the CTA's slot.
   __syncthreads();   // every warp's buffers are final
-  if (m <= 4) {
-    for (int tk = 0; tk < m; ++tk) compact(CC, tk, K);
-    __syncthreads();
-    for (int tk = warp; tk < m; tk += W) {
-      const int len = lane < W ? (int)ccnt[lane * m + tk] : 0;
-      const unsigned long long mine =
-          merge_lists(cbuf + ((size_t)(lane < W ? lane : 0) * m + tk) * p.cap, len, K);
-      if (lane < K) a.cand[((size_t)tk * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
-    }
-  } else {
-    for (int tk = warp; tk < m; tk += W) {
-      unsigned long long e[W];
+  for (int tk = warp; tk < m; tk += W) {
+    unsigned long long e[W];
 #pragma unroll
-      for (int i = 0; i < W; ++i) {
-        const int c = (int)min(ccnt[i * m + tk], (unsigned int)p.cap);
-        e[i] = lane < c ? cbuf[((size_t)i * m + tk) * p.cap + lane] : kEmptyKey;
-      }
-      const unsigned long long mine = warp_tournament<W>(e, K);
-      if (lane < K) a.cand[((size_t)tk * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
+    for (int i = 0; i < W; ++i) {
+      const int c = (int)min(ccnt[i * m + tk], (unsigned int)p.cap);
+      e[i] = lane < c ? cbuf[((size_t)i * m + tk) * p.cap + lane] : kEmptyKey;
     }
+    const unsigned long long mine = warp_tournament<W>(e, K);
+    if (lane < K) a.cand[((size_t)tk * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
   }
   __syncthreads();
   if (threadIdx.x == 0) *flag = (ticket_add(a.counter) == gridDim.x - 1) ? 1u : 0u;
@@ -937,36 +921,27 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
   // The slots are sorted and hold disjoint rows, so every slot whose first
   // entry is below the K-th largest first entry holds nothing of the final
   // K (K larger keys exist).  Per token: every slot's first entry (one round
-  // trip, staged in the free ring in runs of 32), each run's K best
-  // (compactions), their merge -- the K best first entries -- and the merge
-  // of those K slots.
+  // trip, staged in the free ring), the K best of them (K rounds of a warp
+  // maximum), and the merge of those K slots.
   const int nsrc = (int)gridDim.x;
-  const int nch = (nsrc + 31) / 32;                     // runs of 32 first entries per token
-  unsigned long long* heads = reinterpret_cast<unsigned long long*>(sm + p.off_ring);  // [m][nch][32]
-  unsigned int* hcnt = reinterpret_cast<unsigned int*>(heads + (size_t)m * nch * 32);  // [m][nch]
-  unsigned int* hthr = hcnt + m * nch;
-  const bool staged = nch <= 32 &&
-      (size_t)m * nch * (32 * 8 + 8) <= (size_t)W * kRingBytes;
+  unsigned long long* heads = reinterpret_cast<unsigned long long*>(sm + p.off_ring);  // [m][nsrc]
+  const bool staged = nsrc <= 256 && (size_t)m * nsrc * 8u <= (size_t)W * kRingBytes;
   if (staged) {
-    const int total = m * nch * 32;
+    const int total = m * nsrc;
     constexpr int kB = 8;   // loads per thread in flight
     for (int i0 = threadIdx.x; i0 < total; i0 += kB * kThr) {
       unsigned long long v[kB];
 #pragma unroll
       for (int b = 0; b < kB; ++b) {
         const int i = i0 + b * kThr;
-        const int tk = i / (nch * 32), src = i - tk * nch * 32;
-        v[b] = i < total && src < nsrc
-                   ? __ldcg(a.cand + ((size_t)tk * WQL_MAX_CTAS + src) * K) : kEmptyKey;
+        const int tk = i / nsrc;
+        v[b] = i < total ? __ldcg(a.cand + ((size_t)tk * WQL_MAX_CTAS + (i - tk * nsrc)) * K)
+                         : kEmptyKey;
       }
 #pragma unroll
       for (int b = 0; b < kB; ++b)
         if (i0 + b * kThr < total) heads[i0 + b * kThr] = v[b];
     }
-    for (int i = threadIdx.x; i < m * nch; i += kThr)
-      hcnt[i] = (unsigned int)min(32, nsrc - (i % nch) * 32);
-    __syncthreads();
-    for (int i = warp; i < m * nch; i += W) compact_buf(heads + (size_t)i * 32, hcnt + i, hthr + i, 32, K);
     __syncthreads();
   }
   const int big = p.tex * (p.tpc + 1);   // tiles of the CTAs holding tpc + 1
@@ -974,8 +949,11 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
     const unsigned long long* slots = a.cand + (size_t)tk * WQL_MAX_CTAS * K;
     unsigned long long mine;
     if (staged) {
-      const int c = lane < nch ? tk * nch + lane : 0;
-      const unsigned long long hk = merge_lists(heads + (size_t)c * 32, lane < nch ? (int)hcnt[c] : 0, K);
+      unsigned long long e[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        e[q] = lane + 32 * q < nsrc ? heads[tk * nsrc + lane + 32 * q] : kEmptyKey;
+      const unsigned long long hk = warp_tournament<8>(e, K);
       int sid = -1;            // lane r: the CTA of the r-th best first entry
       if (hk != kEmptyKey) {
         const int tile = key_index(hk) >> 4;

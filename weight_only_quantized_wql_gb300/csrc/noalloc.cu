@@ -131,8 +131,11 @@ extern "C" wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t
   if (st != WQL_OK) return st;
   const int64_t n = w->n, k = w->k;
   if (m == 0 || n == 0) return WQL_OK;
-  const int slice_tokens = decode_max_tokens((int)k, w->bits, (int)g, topk, w->format);
-  if (slice_tokens < 1) return WQL_EUNSUPPORTED;
+  const int max_tokens = decode_max_tokens((int)k, w->bits, (int)g, topk, weight_format(w));
+  if (max_tokens < 1) return WQL_EUNSUPPORTED;
+  // balanced slices (16 tokens that do not fit one launch run as 8 + 8)
+  const int64_t nslices = (m + max_tokens - 1) / max_tokens;
+  const int slice_tokens = (int)((m + nslices - 1) / nslices);
   const int64_t slice_max = m < slice_tokens ? m : slice_tokens;
   // Every slice reuses the same area, so one slice's layout is the need.
   const WorkspaceLayout lay = workspace_layout(slice_max, n, topk);
@@ -160,7 +163,8 @@ extern "C" wql_status wql_logits_noalloc(const void* x, int32_t x_dtype, int64_t
   base.k = (int)k;
   base.bias = bias;
   base.topk = topk;
-  base.format = w->format;
+  base.format = weight_format(w);
+  base.weights_static = (w->format & WQL_WEIGHT_STATIC) ? 1 : 0;
   base.zeros = static_cast<const uint8_t*>(w->zeros);
   base.counter = counter;   // also schedules the decode kernel's work units
   if (topk > 0) {

@@ -115,7 +115,9 @@ wql_status check_logits_args(const void* x, int32_t x_dtype, int64_t m, const wq
                              const void* bias, const void* logits_out, int32_t topk,
                              const void* topk_idx, const void* topk_val, int64_t* g_out) {
   if (!w || m < 0 || w->n < 0 || w->k <= 0 || w->group < 0) return WQL_EINVAL;
-  if (w->format != WQL_FMT_SYM && w->format != WQL_FMT_E4M3 && w->format != WQL_FMT_ASYM)
+  const int fmt = weight_format(w);
+  if ((w->format & ~(WQL_FMT_MASK | WQL_WEIGHT_STATIC)) != 0 ||
+      (fmt != WQL_FMT_SYM && fmt != WQL_FMT_E4M3 && fmt != WQL_FMT_ASYM))
     return WQL_EINVAL;
   if (topk < 0 || topk > WQL_MAX_TOPK) return WQL_EINVAL;
   const int64_t n = w->n, k = w->k;
@@ -125,11 +127,11 @@ wql_status check_logits_args(const void* x, int32_t x_dtype, int64_t m, const wq
     if (!logits_out && topk == 0) return WQL_EINVAL;
     if (topk > 0 && (!topk_idx || !topk_val)) return WQL_EINVAL;
     if (topk > n) return WQL_EINVAL;
-    if (w->format == WQL_FMT_ASYM && !w->zeros) return WQL_EINVAL;
+    if (fmt == WQL_FMT_ASYM && !w->zeros) return WQL_EINVAL;
   }
   if (w->bits != 4 && w->bits != 8) return WQL_EUNSUPPORTED;
-  if (w->format == WQL_FMT_E4M3 && (w->bits != 8 || w->group != 0)) return WQL_EUNSUPPORTED;
-  if (w->format == WQL_FMT_ASYM && (w->bits != 4 || w->group == 0 || w->group % 128 != 0))
+  if (fmt == WQL_FMT_E4M3 && (w->bits != 8 || w->group != 0)) return WQL_EUNSUPPORTED;
+  if (fmt == WQL_FMT_ASYM && (w->bits != 4 || w->group == 0 || w->group % 128 != 0))
     return WQL_EUNSUPPORTED;
   if (!half_dtype(x_dtype) || !half_dtype(w->scale_dtype)) return WQL_EUNSUPPORTED;
   const int64_t g = w->group == 0 ? k : w->group;
@@ -263,7 +265,7 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   const int esz = 2;
   // tokens per decode launch: 16, fewer when x for 16 rows does not fit in
   // shared memory next to the rest
-  const int dchunk = decode_max_tokens((int)k, w->bits, (int)g, topk, w->format);
+  const int dchunk = decode_max_tokens((int)k, w->bits, (int)g, topk, weight_format(w));
   if (dchunk < 1) return WQL_EUNSUPPORTED;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -281,7 +283,8 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   base.k = (int)k;
   base.bias = bias;
   base.topk = topk;
-  base.format = w->format;
+  base.format = weight_format(w);
+  base.weights_static = (w->format & WQL_WEIGHT_STATIC) ? 1 : 0;
   base.zeros = static_cast<const uint8_t*>(w->zeros);
   // the counter block also schedules the decode kernel's work units
   if (ws) base.counter = reinterpret_cast<unsigned int*>(ws + lay.counter_off);
@@ -296,9 +299,12 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
   probe.m = (int)(m < 256 ? m : 256);
   // (fp8 and zero-point weights, and candidates alone, take the decode
   // kernel's 16-token slices at every m)
-  const bool use_tc = m > kDecodeMaxTokens && w->format == WQL_FMT_SYM && logits_out &&
+  const bool use_tc = m > kDecodeMaxTokens && weight_format(w) == WQL_FMT_SYM && logits_out &&
                       tc_supported(probe);
-  const int64_t chunk = use_tc ? 256 : dchunk;
+  // decode slices of balanced size (16 tokens that do not fit one launch run
+  // as 8 + 8, not 15 + 1: the weight is streamed once per slice either way)
+  const int64_t nslices = (m + dchunk - 1) / dchunk;
+  const int64_t chunk = use_tc ? 256 : (m + nslices - 1) / nslices;
   for (int64_t m0 = 0; m0 < m; m0 += chunk) {
     const int64_t mc = (m - m0) < chunk ? (m - m0) : chunk;
     LogitsArgs a = base;
@@ -327,9 +333,11 @@ wql_status wql_logits(const void* x, int32_t x_dtype, int64_t m, const wql_weigh
 wql_status wql_embed_gather(const int32_t* ids, int64_t t, const wql_weight* w,
                             int32_t out_dtype, void* out, cudaStream_t stream) {
   if (!w || t < 0 || w->n < 0 || w->k <= 0 || w->group < 0) return WQL_EINVAL;
-  if (w->format != WQL_FMT_SYM && w->format != WQL_FMT_E4M3 && w->format != WQL_FMT_ASYM)
+  const int fmt = weight_format(w);
+  if ((w->format & ~(WQL_FMT_MASK | WQL_WEIGHT_STATIC)) != 0 ||
+      (fmt != WQL_FMT_SYM && fmt != WQL_FMT_E4M3 && fmt != WQL_FMT_ASYM))
     return WQL_EINVAL;
-  if (w->format != WQL_FMT_SYM) return WQL_EUNSUPPORTED;
+  if (fmt != WQL_FMT_SYM) return WQL_EUNSUPPORTED;
   const int64_t n = w->n, k = w->k;
   if (t > 0 && (!ids || !out)) return WQL_EINVAL;
   if (t > 0 && n > 0 && (!w->qweight || !w->scales)) return WQL_EINVAL;

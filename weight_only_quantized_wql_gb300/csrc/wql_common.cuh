@@ -471,6 +471,9 @@ struct LogitsArgs {
 long long diag_wait_budget();
 int diag_stall_mma();
 
+// The code format of a weight (wql_weight.format without its flag bits).
+inline int weight_format(const wql_weight* w) { return w->format & WQL_FMT_MASK; }
+
 // Host checks shared by the logits entry points (no CUDA call): argument
 // validity, the weight's format, sizes and alignment.  On WQL_OK, *g_out is
 // the effective group (k for one scale per row).
