@@ -132,12 +132,6 @@ __device__ __forceinline__ uint32_t ldg_scale2(const uint16_t* p) {
   return v;
 }
 
-__device__ __forceinline__ void griddep_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // Code conversion per variant: fp16 int4 reads the high nibble of each byte
 // in place (x pre-scaled by 1/16 there); everything else uses OffsetCodes.
@@ -997,17 +991,7 @@ cudaError_t launch_t(const DecodeParams& p, size_t smem, int ctas, cudaStream_t 
     if (e != cudaSuccess) return e;
     carveout = pct;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ctas);
-  cfg.blockDim = dim3(warps_of(NT) * 32);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  const cudaError_t e = launch_pdl(kern, dim3((unsigned)ctas), dim3(warps_of(NT) * 32), smem, s, p);
   note_launch();
   return e;
 }

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(WQL_MAX_TOPK * 32) rescore_kernel(const Rescor
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = a.topk;
+  griddep_launch_dependents();
+  griddep_wait();   // the candidates and logits of the kernels before it
   if (warp < K) {
     const int idx = a.topk_idx[(size_t)row * K + warp];
     if (idx < 0 || idx >= a.n) {
@@ -69,12 +71,12 @@ __global__ void __launch_bounds__(WQL_MAX_TOPK * 32) rescore_kernel(const Rescor
 
 cudaError_t launch_rescore(const RescoreArgs& a, cudaStream_t s) {
   const int threads = a.topk * 32;
-  if (a.x_dtype == WQL_F16)
-    rescore_kernel<__half><<<a.m, threads, 0, s>>>(a);
-  else
-    rescore_kernel<__nv_bfloat16><<<a.m, threads, 0, s>>>(a);
+  const cudaError_t e =
+      a.x_dtype == WQL_F16
+          ? launch_pdl(rescore_kernel<__half>, dim3(a.m), dim3(threads), 0, s, a)
+          : launch_pdl(rescore_kernel<__nv_bfloat16>, dim3(a.m), dim3(threads), 0, s, a);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace wql

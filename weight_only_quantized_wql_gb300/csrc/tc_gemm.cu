@@ -241,6 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // barriers and tensor memory are set up; from here on the kernel reads its
+  // inputs and the workspace and writes its outputs
+  griddep_launch_dependents();
+  griddep_wait();
   const uint32_t tmem_base = *tmem_slot;
   bool bad = false;
 
@@ -662,9 +666,9 @@ cudaError_t tc_launch_t(const CUtensorMap& tw, const CUtensorMap& tx, const TcPa
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  kern<<<ctas, kThreads, smem, s>>>(tw, tx, p);
+  const cudaError_t e = launch_pdl(kern, dim3((unsigned)ctas), dim3(kThreads), smem, s, tw, tx, p);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

@@ -323,6 +323,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const LogitsAr
     S.thresh = 0u;
     S.nbest = 0u;
   }
+  griddep_launch_dependents();
+  griddep_wait();   // the logits kernel before it has finished
   // ---- this range's candidates ----
   // Queue every position with key >= thresh; `keys_of(l)` gives this
   // thread's l-th group of 8 raw logits of the current step.
@@ -556,9 +558,9 @@ cudaError_t launch_t(const LogitsArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  kern<<<dim3(a.m, parts), kThreads, smem, s>>>(a, parts);
+  const cudaError_t e = launch_pdl(kern, dim3(a.m, parts), dim3(kThreads), smem, s, a, parts);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

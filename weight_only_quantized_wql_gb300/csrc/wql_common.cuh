@@ -425,6 +425,39 @@ __device__ __forceinline__ unsigned long long pick(const unsigned long long (&v)
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: the kernels of the logits path (decode,
+// tensor-core, top-K selection, rescoring) are launched so that each may
+// start while the preceding kernel on the stream finishes; each reads
+// nothing another kernel may write (its inputs, the workspace) and writes
+// nothing before griddep_wait(), which returns once the preceding kernel has
+// completed and its writes are visible (the decode kernel's early weight
+// copies under WQL_WEIGHT_STATIC are the one documented exception).
+// griddep_launch_dependents() lets the following kernel launch early.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// ---------------------------------------------------------------------------
 // Internal launchers
 // ---------------------------------------------------------------------------
 struct QuantizeArgs {
