@@ -315,3 +315,32 @@ def test_embed_gather_shapes():
     want = oracle.embed_gather(ids.reshape(-1).numpy(), o_qw, 4, o_s, oracle.F16, 64, n, k,
                                oracle.F16)
     assert np.array_equal(np_bits(out.reshape(6, k)), want)
+
+
+@pytest.mark.parametrize("scheme", [SCHEMES[0], SCHEMES[4], SCHEMES[1]],
+                         ids=lambda s: f"w{s[0]}g{s[1]}s{s[2]}")
+def test_static_weights_back_to_back(scheme):
+    """WQL_WEIGHT_STATIC: the decode kernel copies the weight before the
+    preceding kernel on the stream has finished.  Calls issued back to back
+    (each one's X written by a copy kernel right before it) give exactly the
+    results of calls without the flag, and match the oracle."""
+    n, k, K = 4099, 512, 8
+    bits, group, sdt, wdt, xdt, clip = scheme
+    w, qw, o_qw, o_s = _make(n, k, scheme, seed=21)
+    qs = wql.QuantizedWeight(qw.qweight, qw.scales, qw.bits, qw.group, qw.n, qw.k, static=True)
+    ws1, ws2 = wql.Workspace(DEV), wql.Workspace(DEV)
+    for m in (1, 4, 16):
+        xs = [synth.activations(m, k, xdt, seed=600 + 10 * m + i) for i in range(4)]
+        xd = torch.empty(m, k, dtype=TORCH_OF[xdt], device=DEV)
+        outs = []
+        for x in xs:              # copy X in, then the static call, back to back
+            xd.copy_(x.to(DEV), non_blocking=True)
+            outs.append(tuple(t.clone() for t in wql.wql_logits(xd, qs, topk=K, workspace=ws1)))
+        torch.cuda.synchronize()
+        for x, (lg, idx, val) in zip(xs, outs):
+            rl, ri, rv = wql.wql_logits(x.to(DEV), qw, topk=K, workspace=ws2)
+            torch.cuda.synchronize()
+            assert torch.equal(lg, rl) and torch.equal(idx, ri) and torch.equal(val, rv)
+        ref, absacc = oracle.logits(np_input(xs[-1], xdt), xdt, o_qw, bits, o_s, sdt, group, n, k,
+                                    nthreads=4)
+        assert_logits_close(to_f64(outs[-1][0]), ref, absacc, f"static m={m}")
