@@ -344,3 +344,25 @@ def test_static_weights_back_to_back(scheme):
         ref, absacc = oracle.logits(np_input(xs[-1], xdt), xdt, o_qw, bits, o_s, sdt, group, n, k,
                                     nthreads=4)
         assert_logits_close(to_f64(outs[-1][0]), ref, absacc, f"static m={m}")
+
+
+@pytest.mark.parametrize("m", [9, 16])
+def test_logits_long_rows_many_tokens(m):
+    """k = 5120 with up to 16 bf16 token rows: X for 16 rows (160 KB) does
+    not fit in shared memory next to the rings, so the rows run as balanced
+    slices (8 + 8, or 5 + 4)."""
+    n, k, K = 4099, 5120, 8
+    scheme = (4, 128, oracle.BF16, oracle.BF16, oracle.BF16, 0)
+    bits, group, sdt, wdt, xdt, clip = scheme
+    w, qw, o_qw, o_s = _make(n, k, scheme, seed=31)
+    x = synth.activations(m, k, xdt, seed=700 + m)
+    n0 = wql.wql_launch_count()
+    logits, idx, val = wql.wql_logits(x.to(DEV), qw, topk=K)
+    torch.cuda.synchronize()
+    assert wql.wql_launch_count() - n0 == 2, "two balanced decode slices"
+    ref, absacc = oracle.logits(np_input(x, xdt), xdt, o_qw, bits, o_s, sdt, group, n, k,
+                                nthreads=8)
+    assert_logits_close(to_f64(logits), ref, absacc, f"long rows m={m}")
+    g_idx, g_val = idx.cpu().numpy(), val.cpu().numpy()
+    ties = sum(check_topk(g_idx[r], g_val[r], ref[r], absacc[r], K) for r in range(m))
+    report_ties(f"long rows m={m}", ties, m)
