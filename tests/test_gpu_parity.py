@@ -359,7 +359,7 @@ def test_logits_long_rows_many_tokens(m):
     n0 = wql.wql_launch_count()
     logits, idx, val = wql.wql_logits(x.to(DEV), qw, topk=K)
     torch.cuda.synchronize()
-    assert wql.wql_launch_count() - n0 == 2, "two balanced decode slices"
+    assert wql.wql_launch_count() - n0 == (1 if m <= 15 else 2), "balanced decode slices"
     ref, absacc = oracle.logits(np_input(x, xdt), xdt, o_qw, bits, o_s, sdt, group, n, k,
                                 nthreads=8)
     assert_logits_close(to_f64(logits), ref, absacc, f"long rows m={m}")
