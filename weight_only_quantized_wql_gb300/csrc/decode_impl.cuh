@@ -252,30 +252,72 @@ __device__ __forceinline__ void warp_topk_of(int count, int K, Load load,
   warp_merge_topk_redux<KT>(list, K, out);
 }
 
-// The K best of keys spread over a warp, E per lane (unique but for
-// kEmptyKey), by K rounds of a warp-wide maximum (two hardware reductions:
-// value half, then index half among the lanes holding that value); the
-// lane holding a round's winner removes it.  The r-th best ends on lane r.
+// The largest of a lane's E keys (E a power of two) and its position, by a
+// tree of comparisons: log2(E) levels of independent compare-selects instead
+// of one chain of E.
+template <int E>
+__device__ __forceinline__ void lane_max(const unsigned long long (&e)[E], unsigned long long& best,
+                                         int& at) {
+  unsigned long long v[E];
+  int ix[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    v[i] = e[i];
+    ix[i] = i;
+  }
+#pragma unroll
+  for (int w = E / 2; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const bool gt = v[i + w] > v[i];
+      v[i] = gt ? v[i + w] : v[i];
+      ix[i] = gt ? ix[i + w] : ix[i];
+    }
+  best = v[0];
+  at = ix[0];
+}
+
+// The K best of keys spread over a warp, E per lane (E a power of two; keys
+// unique but for kEmptyKey), by K rounds of a warp-wide maximum (two
+// hardware reductions: value half, then index half among the lanes holding
+// that value).  Every lane runs every round's update, predicated on holding
+// the winner (no divergent branch: a lone winner lane would expose the whole
+// update's latency): it clears the winner and finds its next largest -- by a
+// tree for E <= 8, by one pass for E = 16 (fewer instructions there).  The
+// r-th best ends on lane r.
 template <int E>
 __device__ __forceinline__ unsigned long long warp_tournament(unsigned long long (&e)[E], int K) {
+  static_assert((E & (E - 1)) == 0, "E is a power of two");
   const int lane = threadIdx.x & 31;
-  unsigned long long best = e[0];
+  unsigned long long best;
+  int at = 0;
+  if constexpr (E >= 16) {
+    best = e[0];
 #pragma unroll
-  for (int i = 1; i < E; ++i) best = e[i] > best ? e[i] : best;
+    for (int i = 1; i < E; ++i) best = e[i] > best ? e[i] : best;
+  } else {
+    lane_max<E>(e, best, at);
+  }
   unsigned long long mine = kEmptyKey;
   for (int r = 0; r < K; ++r) {
     const uint32_t hi = (uint32_t)(best >> 32);
     const uint32_t mh = redux_max_u32(hi);
     const uint32_t ml = redux_max_u32(hi == mh ? (uint32_t)best : 0u);
     const unsigned long long top = ((unsigned long long)mh << 32) | ml;
-    if (lane == r) mine = top;
-    if (best == top && top != kEmptyKey) {
-      best = kEmptyKey;
+    mine = lane == r ? top : mine;
+    const bool win = best == top;   // (with top empty: clears only empties)
+    if constexpr (E >= 16) {
+      unsigned long long nb = kEmptyKey;
 #pragma unroll
       for (int i = 0; i < E; ++i) {
-        if (e[i] == top) e[i] = kEmptyKey;
-        best = e[i] > best ? e[i] : best;
+        e[i] = win && e[i] == top ? kEmptyKey : e[i];
+        nb = e[i] > nb ? e[i] : nb;
       }
+      best = nb;
+    } else {
+#pragma unroll
+      for (int i = 0; i < E; ++i) e[i] = win && i == at ? kEmptyKey : e[i];
+      lane_max<E>(e, best, at);
     }
   }
   return mine;
@@ -283,7 +325,8 @@ __device__ __forceinline__ unsigned long long warp_tournament(unsigned long long
 
 // The K best of up to 32 sorted lists (descending, kEmptyKey-padded), lane
 // l holding list l in registers: K rounds of a warp maximum over the lists'
-// heads; the winning lane shifts its list.  The r-th best ends on lane r.
+// heads; the winning lane shifts its list (a predicated shift, no branch).
+// The r-th best ends on lane r.
 template <int KT>
 __device__ __forceinline__ unsigned long long warp_merge_lists(unsigned long long (&lst)[KT],
                                                                int K) {
@@ -295,12 +338,11 @@ __device__ __forceinline__ unsigned long long warp_merge_lists(unsigned long lon
     const uint32_t mh = redux_max_u32(hi);
     const uint32_t ml = redux_max_u32(hi == mh ? (uint32_t)head : 0u);
     const unsigned long long top = ((unsigned long long)mh << 32) | ml;
-    if (lane == r) mine = top;
-    if (head == top && top != kEmptyKey) {
+    mine = lane == r ? top : mine;
+    const bool win = head == top && top != kEmptyKey;   // the list to shift (branch-free)
 #pragma unroll
-      for (int i = 0; i < KT - 1; ++i) lst[i] = lst[i + 1];
-      lst[KT - 1] = kEmptyKey;
-    }
+    for (int i = 0; i < KT - 1; ++i) lst[i] = win ? lst[i + 1] : lst[i];
+    lst[KT - 1] = win ? kEmptyKey : lst[KT - 1];
   }
   return mine;
 }
