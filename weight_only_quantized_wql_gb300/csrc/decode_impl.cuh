@@ -721,22 +721,30 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
         for (int c = 0; c < 4; ++c)
           pass[nt][c] = pass[nt][c] && (uint32_t)(key[nt][c] >> 32) >= thr[nt][c & 1];
     }
-    // appends, one shared atomic per (value slot, token): lanes of one token
-    // within a value slot share t
+    // appends: the two value slots of a token (rows g and g + 8: c = h and
+    // h + 2) go to its buffer with one count read (a broadcast) and one count
+    // write by the group's first lane; no atomics -- only this warp touches
+    // its buffers and counts until the end of its runs
+    const unsigned int lt = (1u << lane) - 1u;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (GW2 && (c & 1)) continue;
-        const unsigned int pm = __ballot_sync(0xFFFFFFFFu, pass[nt][c]);
-        if (pm == 0u) continue;
-        const int tok = GW2 ? (t + 4 * nt) : (8 * nt + 2 * t + (c & 1));
-        const unsigned int peers = pm & (0x11111111u << t);   // same t, passing
-        const int leader = peers ? __ffs(peers) - 1 : 0;
-        unsigned int base = 0u;
-        if (pass[nt][c] && lane == leader) base = atomicAdd(&CC.cnt[tok], (unsigned int)__popc(peers));
-        base = __shfl_sync(0xFFFFFFFFu, base, leader);
-        if (pass[nt][c]) CC.buf[tok * CC.cap + base + __popc(peers & ((1u << lane) - 1u))] = key[nt][c];
+      for (int h = 0; h < (GW2 ? 1 : 2); ++h) {
+        const unsigned int pa = __ballot_sync(0xFFFFFFFFu, pass[nt][h]);
+        const unsigned int pb = __ballot_sync(0xFFFFFFFFu, pass[nt][h + 2]);
+        if ((pa | pb) == 0u) continue;                       // (warp-uniform)
+        const int tok = GW2 ? (t + 4 * nt) : (8 * nt + 2 * t + h);
+        const unsigned int grp = 0x11111111u << t;           // lanes of this token (same t)
+        const unsigned int na = __popc(pa & grp), nb = __popc(pb & grp);
+        const bool any_t = tok < m && na + nb != 0u;
+        const unsigned int base = any_t ? CC.cnt[tok] : 0u;
+        __syncwarp();                                        // every read before the write
+        if (any_t) {
+          unsigned long long* dst = CC.buf + tok * CC.cap + base;
+          if (pass[nt][h]) dst[__popc(pa & grp & lt)] = key[nt][h];
+          if (pass[nt][h + 2]) dst[na + __popc(pb & grp & lt)] = key[nt][h + 2];
+          if (lane == t) CC.cnt[tok] = base + na + nb;
+        }
       }
     __syncwarp();
   };
