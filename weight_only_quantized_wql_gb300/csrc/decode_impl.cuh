@@ -347,6 +347,34 @@ __device__ __forceinline__ unsigned long long warp_merge_lists(unsigned long lon
   return mine;
 }
 
+// Merge of two sorted lists of K <= 16 keys (best first, kEmptyKey padded,
+// keys unique but for kEmptyKey; shared memory) into their K best, best
+// first, returned on lanes 0..K-1 and left at out (which may be A): lanes
+// 0..15 hold A, lanes 16..31 hold B, each key's rank is its index plus the
+// keys of the other list above it (16 shuffles, no rounds), and each key
+// below rank K is written at its rank.
+__device__ __forceinline__ unsigned long long warp_merge2(const unsigned long long* A,
+                                                          const unsigned long long* B, int K,
+                                                          unsigned long long* out) {
+  const int lane = threadIdx.x & 31;
+  const int i = lane & 15;
+  const unsigned long long x = i < K ? (lane < 16 ? A[i] : B[i]) : kEmptyKey;
+  int r = i;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int src = lane < 16 ? 16 + j : j;
+    const uint32_t lo = __shfl_sync(0xFFFFFFFFu, (uint32_t)x, src);
+    const uint32_t hi = __shfl_sync(0xFFFFFFFFu, (uint32_t)(x >> 32), src);
+    r += (((unsigned long long)hi << 32) | lo) > x ? 1 : 0;
+  }
+  __syncwarp();
+  if (lane < K) out[lane] = kEmptyKey;
+  __syncwarp();
+  if (x != kEmptyKey && r < K) out[r] = x;
+  __syncwarp();
+  return lane < K ? out[lane] : kEmptyKey;
+}
+
 // Ticket of the last-CTA merge: an atomic add whose release makes this CTA's
 // slot writes and threshold update (ordered before it by the preceding block
 // barrier) visible before the ticket, and whose acquire, for the last CTA,
@@ -942,19 +970,44 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
 
   // ---- top-K of this CTA ----
   // Every warp's buffer holds, per token, all of its values that can be
-  // among its K best.  Warp tk takes the K best of the W buffers of token tk
-  // at once (lane l holds entry l of every buffer: K rounds of a warp
-  // maximum) and writes them, best first, to the CTA's slot.
+  // among its K best.  The K best of the W buffers of a token (lane l holds
+  // entry l of every buffer: K rounds of a warp maximum) -- with enough
+  // warps, two warps take half of the buffers each and one merges their two
+  // sorted lists -- go, best first, to the CTA's slot.
   __syncthreads();   // every warp's buffers are final
-  for (int tk = warp; tk < m; tk += W) {
-    unsigned long long e[W];
+  if (2 * m <= W) {
+    // two warps per token, each over half of the buffers, then one merge
+    constexpr int H = W / 2;
+    unsigned long long* half_best = reinterpret_cast<unsigned long long*>(sm + p.off_ring);  // [m][2][16]
+    if (warp < 2 * m) {
+      const int tk = warp >> 1, part = warp & 1;
+      unsigned long long e[H];
 #pragma unroll
-    for (int i = 0; i < W; ++i) {
-      const int c = (int)min(ccnt[i * m + tk], (unsigned int)p.cap);
-      e[i] = lane < c ? cbuf[((size_t)i * m + tk) * p.cap + lane] : kEmptyKey;
+      for (int i = 0; i < H; ++i) {
+        const int b = part * H + i;
+        const int c = (int)min(ccnt[b * m + tk], (unsigned int)p.cap);
+        e[i] = lane < c ? cbuf[((size_t)b * m + tk) * p.cap + lane] : kEmptyKey;
+      }
+      const unsigned long long mine = warp_tournament<H>(e, K);
+      if (lane < 16) half_best[(tk * 2 + part) * 16 + lane] = lane < K ? mine : kEmptyKey;
     }
-    const unsigned long long mine = warp_tournament<W>(e, K);
-    if (lane < K) a.cand[((size_t)tk * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
+    __syncthreads();
+    for (int tk = warp; tk < m; tk += W) {
+      const unsigned long long mine =
+          warp_merge2(half_best + tk * 32, half_best + tk * 32 + 16, K, half_best + tk * 32);
+      if (lane < K) a.cand[((size_t)tk * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
+    }
+  } else {
+    for (int tk = warp; tk < m; tk += W) {
+      unsigned long long e[W];
+#pragma unroll
+      for (int i = 0; i < W; ++i) {
+        const int c = (int)min(ccnt[i * m + tk], (unsigned int)p.cap);
+        e[i] = lane < c ? cbuf[((size_t)i * m + tk) * p.cap + lane] : kEmptyKey;
+      }
+      const unsigned long long mine = warp_tournament<W>(e, K);
+      if (lane < K) a.cand[((size_t)tk * WQL_MAX_CTAS + blockIdx.x) * K + lane] = mine;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) *flag = (ticket_add(a.counter) == gridDim.x - 1) ? 1u : 0u;
