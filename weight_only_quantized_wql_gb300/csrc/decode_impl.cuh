@@ -732,14 +732,32 @@ __global__ void __launch_bounds__(warps_of(NT) * 32, 1)
       }
     }
     if (K <= 0 || !__any_sync(0xFFFFFFFFu, any)) return;
-    // make room: a token whose buffer could overflow with this tile is
-    // compacted first (raising its threshold), then the values re-checked
-    bool compacted = false;
-    for (int tk = 0; tk < m; ++tk) {
-      if (CC.cnt[tk] + 16u > (unsigned int)CC.cap) {
-        compact(CC, tk, K);
-        compacted = true;
+    // make room: a token whose buffer would overflow with this tile's
+    // passing values is compacted first (raising its threshold), then the
+    // values are re-checked (passes only become fewer)
+    unsigned int need = 0u;   // tokens to compact (warp-uniform)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < (GW2 ? 1 : 2); ++h) {
+        // this tile's passing values of the tokens of (nt, h): lanes of one
+        // token share t
+        const unsigned int pa = __ballot_sync(0xFFFFFFFFu, pass[nt][h]);
+        const unsigned int pb = __ballot_sync(0xFFFFFFFFu, pass[nt][h + 2]);
+        if ((pa | pb) == 0u) continue;
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) {
+          const int tok = GW2 ? (tq + 4 * nt) : (8 * nt + 2 * tq + h);
+          const unsigned int grp = 0x11111111u << tq;
+          const unsigned int np = __popc(pa & grp) + __popc(pb & grp);
+          if (tok < m && np != 0u && CC.cnt[tok] + np > (unsigned int)CC.cap) need |= 1u << tok;
+        }
       }
+    const bool compacted = need != 0u;
+    while (need) {
+      const int tk = __ffs(need) - 1;
+      need &= need - 1u;
+      compact(CC, tk, K);
     }
     if (compacted) {
       load_thr();
