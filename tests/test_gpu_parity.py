@@ -252,16 +252,17 @@ def _rowwise_weight(n, k, row_value):
 
 
 @pytest.mark.parametrize("m", [1, 4, 32, 256])
-@pytest.mark.parametrize("order", ["increasing", "decreasing", "equal"])
+@pytest.mark.parametrize("order", ["increasing", "decreasing", "equal", "negative"])
 def test_tensor_core_topk_adversarial_orders(m, order):
     """Logits that grow with the row index put the best rows last; decreasing
-    ones put them first; equal logits must give the lowest indices, and every
+    ones put them first; negative ones (growing) give a negative selection
+    threshold; equal logits must give the lowest indices, and every
     row ties with the threshold, so the thresholded candidate lists overflow
     and the exhaustive selection runs (decode kernel for m <= 16, selection
     kernel after the tensor-core kernel above)."""
     n, k, K = 40000, 128, 8
     f = {"increasing": lambda r: 0.01 + 1e-5 * r, "decreasing": lambda r: 0.5 - 1e-5 * r,
-         "equal": lambda r: 0.02}[order]
+         "equal": lambda r: 0.02, "negative": lambda r: -0.5 + 1e-5 * r}[order]
     w = _rowwise_weight(n, k, f)
     qw = wql.wql_quantize(w.to(DEV), 4, 64, torch.float16, 0)
     o_qw, o_s = oracle_quantized(w, oracle.F32, 4, 64, oracle.F16, 0)

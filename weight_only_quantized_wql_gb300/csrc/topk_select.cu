@@ -16,8 +16,11 @@
 // range):
 //  * threshold: the K-th largest of 16 half-warp maxima over the range's
 //    first step -- K distinct positions lie at or above it, so it bounds the
-//    range's K-th largest key from below;
-//  * every position with key >= threshold is queued, the range's K-th
+//    range's K-th largest key from below; during the scan it rises to the
+//    K-th largest key that any one warp has queued (again K distinct
+//    positions at or above it);
+//  * every position with key >= threshold is queued (a thread first tests
+//    its 32 logits of a step at once: per-half signed maxima), the range's K-th
 //    largest queued key h_r found, and the positions with key >= h_r -- a
 //    superset of the range's top K, and of its share of the row's top K --
 //    recomputed in fp32 (a warp per position); the range's best K go to the
@@ -76,15 +79,32 @@ __device__ __forceinline__ unsigned int raw_half(const uint4& v, int e) {
 }
 
 
-// Whether any of the 8 rounded logits in v reaches a non-negative
-// threshold pattern t (t2 = t in both halves): a half h passes iff it is
-// positive and h >= t, i.e. iff bit 15 of ((w | 0x8000) - t) & ~w -- the
-// subtraction never borrows across halves since h | 0x8000 >= t.  Three
-// integer operations per two logits.
-__device__ __forceinline__ bool any_ge_pos(const uint4& v, uint32_t t2) {
-  const uint32_t hit = (((v.x | 0x80008000u) - t2) & ~v.x) | (((v.y | 0x80008000u) - t2) & ~v.y) |
-                       (((v.z | 0x80008000u) - t2) & ~v.z) | (((v.w | 0x80008000u) - t2) & ~v.w);
-  return (hit & 0x80008000u) != 0u;
+// Whether any of the thread's kLoads x 8 rounded logits in cur reaches a
+// non-negative threshold key (t = its low 15 bits).  Non-negative fp16 and
+// bf16 patterns order like signed 16-bit integers and negative ones read as
+// negative integers, so the per-half signed maximum clamped at 0 (three
+// inputs per instruction) holds the largest non-negative pattern of each half
+// lane; a NaN with the sign bit clear counts as above +inf, as its key does.
+// Exact for every non-negative threshold.
+__device__ __forceinline__ bool any_reaches_pos(const uint4 (&cur)[kLoads], uint32_t t) {
+  static_assert(kLoads == 4, "the maximum tree below takes 16 words");
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(&cur[0]);
+  const uint32_t m0 = __vimax3_s16x2_relu(w[0], w[1], w[2]);
+  const uint32_t m1 = __vimax3_s16x2_relu(w[3], w[4], w[5]);
+  const uint32_t m2 = __vimax3_s16x2_relu(w[6], w[7], w[8]);
+  const uint32_t m3 = __vimax3_s16x2_relu(w[9], w[10], w[11]);
+  const uint32_t m4 = __vimax3_s16x2_relu(w[12], w[13], w[14]);
+  const uint32_t m5 = __vimax3_s16x2_relu(m0, m1, w[15]);
+  const uint32_t m = __vimax3_s16x2_relu(m2, m3, __vimax_s16x2_relu(m4, m5));
+  return max(m & 0xFFFFu, m >> 16) >= t;
+}
+
+// Bit 15 (low half) and bit 31 (high half) set where a rounded logit of the
+// word w has a key >= a non-negative threshold key (t2 = its low 15 bits in
+// both halves): the half is non-negative and (h | 0x8000) - t keeps bit 15.
+// The subtraction never borrows across halves since h | 0x8000 >= t.
+__device__ __forceinline__ uint32_t reach_bits_pos(uint32_t w, uint32_t t2) {
+  return (((w | 0x80008000u) - t2) & ~w) & 0x80008000u;
 }
 
 struct Hist {
@@ -183,6 +203,7 @@ struct SelShared {
   Hist H;
   unsigned int count, thresh, last, nbest, nlive;
   unsigned int hmax[2 * kWarps];            // half-warp maxima of the first step
+  unsigned int wkth[kWarps];                // each warp's K-th largest queued key
   unsigned long long best[WQL_MAX_TOPK];    // running fp32 top-K, descending
   unsigned int queue[kCap];                 // positions
   unsigned short qkey[kCap];                // their keys
@@ -193,6 +214,24 @@ struct SelShared {
 // The need-th largest of cnt keys qkey[0..cnt) (block-wide; every thread
 // returns it).
 __device__ unsigned int queued_kth(SelShared& S, int cnt, unsigned int need) {
+  if (cnt <= 32) {
+    // one key per lane: the need-th largest is the smallest key with fewer
+    // than `need` keys strictly above it
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      const unsigned int mine = lane < cnt ? (unsigned int)S.qkey[lane] : 0u;
+      unsigned int above = 0u;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) above += __shfl_sync(0xFFFFFFFFu, mine, j) > mine ? 1u : 0u;
+      const unsigned int h =
+          __reduce_min_sync(0xFFFFFFFFu, (lane < cnt && above < need) ? mine : 0xFFFFFFFFu);
+      if (lane == 0) S.thresh = h == 0xFFFFFFFFu ? 0u : h;
+    }
+    __syncthreads();
+    const unsigned int h = S.thresh;
+    __syncthreads();
+    return h;
+  }
   if (cnt <= 32 * kWarpKeys) {
     if (threadIdx.x < 32) {
       const unsigned int h =
@@ -322,31 +361,87 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const LogitsAr
     S.count = 0u;
     S.thresh = 0u;
     S.nbest = 0u;
+    S.bad = 0u;
   }
+  if (threadIdx.x < kWarps) S.wkth[threadIdx.x] = 0u;
   griddep_launch_dependents();
   griddep_wait();   // the logits kernel before it has finished
   // ---- this range's candidates ----
   // Queue every position with key >= thresh; `keys_of(l)` gives this
   // thread's l-th group of 8 raw logits of the current step.
-  auto queue_step = [&](int base, unsigned int thresh, unsigned int t2,
-                        const uint4 (&cur)[kLoads]) {
+  // Queue every position whose key reaches thresh; each thread returns the
+  // largest key it queued (0 if none).
+  auto queue_step = [&](int base, unsigned int thresh, const uint4 (&cur)[kLoads]) -> unsigned int {
+    unsigned int top = 0u;
+    auto enqueue = [&](int pos, unsigned int key) {
+      const unsigned int at = atomicAdd(&S.count, 1u);
+      if (at < (unsigned int)kCap) {
+        S.queue[at] = (unsigned int)pos;
+        S.qkey[at] = (unsigned short)key;
+      }
+      top = max(top, key);
+    };
+    if (thresh >= 0x8000u) {
+      // the common case: nothing of the thread's 32 logits reaches it
+      const uint32_t t = thresh & 0x7FFFu;
+      if (!any_reaches_pos(cur, t)) return 0u;
+      const uint32_t t2 = t * 0x10001u;
 #pragma unroll
-    for (int l = 0; l < kLoads; ++l) {
-      // the common case: a non-negative threshold and nothing in these 8
-      if (thresh >= 0x8000u && !any_ge_pos(cur[l], t2)) continue;
+      for (int l = 0; l < kLoads; ++l) {
+        const uint32_t wv[4] = {cur[l].x, cur[l].y, cur[l].z, cur[l].w};
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) {
-        const int pos = base + (l * kThreads + threadIdx.x) * kPer + e;
-        const unsigned int key = key16(raw_half(cur[l], e));
-        if (pos < hi && key >= thresh) {
-          const unsigned int at = atomicAdd(&S.count, 1u);
-          if (at < (unsigned int)kCap) {
-            S.queue[at] = (unsigned int)pos;
-            S.qkey[at] = (unsigned short)key;
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t hit = reach_bits_pos(wv[i], t2);
+          if (hit == 0u) continue;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int pos = base + (l * kThreads + threadIdx.x) * kPer + 2 * i + h;
+            if (((hit >> (16 * h + 15)) & 1u) != 0u && pos < hi)
+              enqueue(pos, ((wv[i] >> (16 * h)) & 0xFFFFu) | 0x8000u);
           }
         }
       }
+    } else {
+      // a negative threshold: every key is tested
+#pragma unroll
+      for (int l = 0; l < kLoads; ++l) {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+          const int pos = base + (l * kThreads + threadIdx.x) * kPer + e;
+          const unsigned int key = key16(raw_half(cur[l], e));
+          if (pos < hi && key >= thresh) enqueue(pos, key);
+        }
+      }
     }
+    return top;
+  };
+  // The selection threshold rises during the scan: each warp keeps, in lanes
+  // 0 .. need-1, the need largest keys its threads have queued (at most one
+  // per thread and step), sorted descending, and publishes the need-th of
+  // them in S.wkth.  Those are keys of distinct positions of the range, so
+  // each published key, and the largest of them, is a lower bound of the
+  // range's need-th largest key; the published values only grow.
+  unsigned int lst = 0u;
+  auto raise_bound = [&](unsigned int top) {
+    unsigned int hits = __ballot_sync(0xFFFFFFFFu, top != 0u);
+    if (hits == 0u) return;
+    while (hits != 0u) {
+      const int src = __ffs(hits) - 1;
+      hits &= hits - 1u;
+      const unsigned int key = __shfl_sync(0xFFFFFFFFu, top, src);
+      const unsigned int at =
+          (unsigned int)__popc(__ballot_sync(0xFFFFFFFFu, lane < need && lst >= key));
+      const unsigned int up = __shfl_up_sync(0xFFFFFFFFu, lst, 1);
+      if (lane < need && (unsigned int)lane >= at) lst = (unsigned int)lane == at ? key : up;
+    }
+    const unsigned int kth = __shfl_sync(0xFFFFFFFFu, lst, (need - 1) & 31);
+    if (lane == 0) S.wkth[threadIdx.x >> 5] = kth;
+  };
+  auto current_bound = [&](unsigned int t) {
+    const volatile unsigned int* wk = S.wkth;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t = max(t, wk[w]);
+    return t;
   };
   // threshold: need-th largest of the 16 half-warp maxima of the first
   // step (positions >= hi count as key 0, below every real key)
@@ -410,7 +505,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const LogitsAr
         reinterpret_cast<uint4*>(xs)[i] = __ldg(xg + i);
     }
     __syncthreads();
-    unsigned int t2 = 0u;
     for (int st = 0; st < nsteps; ++st) {
       const int b = st % kStages;
       if (!mbar_wait(&S.bar[b], (uint32_t)((st / kStages) & 1))) S.bad = 1u;
@@ -418,10 +512,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const LogitsAr
       const uint4* src = reinterpret_cast<const uint4*>(ring + (size_t)b * kStepBytes);
 #pragma unroll
       for (int l = 0; l < kLoads; ++l) cur[l] = src[l * kThreads + threadIdx.x];
-      if (st == 0) {
-        thresh = first_threshold(cur);     // all warps meet here once
-        t2 = (thresh & 0x7FFFu) * 0x10001u;
-      }
+      if (st == 0) thresh = first_threshold(cur);     // all warps meet here once
       // the step's data is in registers: release the stage; the last warp
       // to release it refills it (no block-wide barrier per step)
       __syncwarp();
@@ -432,7 +523,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const LogitsAr
           if (st + kStages < nsteps) issue(st + kStages);
         }
       }
-      queue_step(lo + st * kStep, thresh, t2, cur);
+      if (st > 0) thresh = current_bound(thresh);
+      raise_bound(queue_step(lo + st * kStep, thresh, cur));
     }
     __syncthreads();
     if (S.bad != 0u) {
@@ -464,7 +556,6 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const LogitsAr
     for (int l = 0; l < kLoads; ++l)
       cur[l] = load_raw(row, hi, lo + (l * kThreads + threadIdx.x) * kPer, false);
     thresh = first_threshold(cur);
-    const unsigned int t2 = (thresh & 0x7FFFu) * 0x10001u;
     for (int base = lo; base < hi; base += kStep) {
       uint4 nxt[kLoads];
 #pragma unroll
@@ -472,7 +563,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const LogitsAr
         nxt[l] = base + kStep < hi
                      ? load_raw(row, hi, base + kStep + (l * kThreads + threadIdx.x) * kPer, false)
                      : make_uint4(0u, 0u, 0u, 0u);
-      queue_step(base, thresh, t2, cur);
+      thresh = current_bound(thresh);
+      raise_bound(queue_step(base, thresh, cur));
 #pragma unroll
       for (int l = 0; l < kLoads; ++l) cur[l] = nxt[l];
     }
